@@ -1,0 +1,232 @@
+/*
+ * fp8z.h -- C ABI of the block-aware ZeRO-1 optimizer step for blockwise-FP8
+ * weights (one GB300, sm_103a).
+ *
+ * Method (pages cited by title and section):
+ *   "A ZeRO Optimizer Design for Blockwise FP8 Quantization" (beipo.top) --
+ *     the weight is quantized per 128x128 block ("Blockwise quantization");
+ *     main params/grads/moments are folded so every 128x128 block is
+ *     contiguous ("Layout transform (fold/unfold)"), then sharded on block
+ *     boundaries ("Block-wise split") or by whole params ("Param-wise split");
+ *     each DP rank updates its shard element-wise and requantizes the new FP8
+ *     weights and scales from its FP32 main params ("Summary").
+ *   lpnh.cn "Model-Optimizer" article, §4.3 -- the AdamW update printed as code.
+ *   "FP8-Flow-MoE: A Casting-Free FP8 Recipe without Double Quantization
+ *     Error", §3.1 -- scale from the block amax and 448, nearest-value rounding,
+ *     the E4M3 value formula, power-of-two scales.
+ *   mhpn.cn "Core scaling strategies in FP8 training", §3.2 (128x128 block
+ *     quantize, scale = 448/amax, clamp to ±448), §4.2 (scale floor 1e-6).
+ *
+ * Conventions for every call:
+ *   - The caller owns all memory.  Device buffers are plain CUDA device
+ *     pointers (for instance from PyTorch); host tables are host pointers.  The
+ *     library allocates no memory.
+ *   - Device calls enqueue work on `stream` (a cudaStream_t; NULL = legacy
+ *     default stream) and return at once.  The return value reports argument
+ *     and launch errors only.  Errors found on the device (a bad block
+ *     descriptor, a wait that ran out of time) are written with an atomic
+ *     compare-and-swap into *dev_status (device int32, must start at 0) when
+ *     the caller passes one; read it after synchronizing the stream.
+ *   - Device pointers must be 16-byte aligned.  A block is 128x128 = 16384
+ *     elements; float buffers hold [nblocks,128,128] fp32 row-major per block,
+ *     byte buffers [nblocks,128,128] E4M3 codes, scale buffers one fp32 per
+ *     block.
+ *   - Return codes are fp8z_status values; fp8z_status_string() names them.
+ */
+#ifndef FP8Z_H
+#define FP8Z_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define FP8Z_BLOCK 128
+#define FP8Z_BLOCK_ELEMS 16384
+
+typedef enum {
+    FP8Z_OK = 0,
+    FP8Z_EINVAL = -1,        /* bad argument (null, negative, out of range)  */
+    FP8Z_EALIGN = -2,        /* pointer not 16-byte aligned                  */
+    FP8Z_ENOSPACE = -3,      /* a range does not fit the stated capacity     */
+    FP8Z_ECUDA = -4,         /* a CUDA runtime call or launch failed         */
+    FP8Z_ETIMEOUT = -5,      /* device: a bounded wait ran out of time       */
+    FP8Z_EUNSUPPORTED = -6   /* no sm_100-family device current              */
+} fp8z_status;
+
+typedef enum { FP8Z_SPLIT_BLOCKWISE = 0, FP8Z_SPLIT_PARAMWISE = 1 } fp8z_split;
+typedef enum { FP8Z_SCALE_EXACT = 0, FP8Z_SCALE_POW2 = 1 } fp8z_scale_mode;
+typedef enum { FP8Z_DECAY_PRE = 0, FP8Z_DECAY_POST = 1 } fp8z_decay_mode;
+
+/* One quantized parameter [e, rows, cols] (e = 1 for a 2-D weight, the expert
+ * count for a 3-D expert bank). */
+typedef struct { int64_t e, rows, cols; } fp8z_param_shape;
+
+/* Planner output per parameter. */
+typedef struct {
+    int64_t blk_offset;      /* first folded block of this param in the flat buffer */
+    int64_t t_offset;        /* first byte of its column-major [e, cols, rows] copy
+                                in a buffer that concatenates all params in order   */
+    int64_t t_scale_offset;  /* first entry of its [e, wb, hb] inverse-scale grid    */
+    int64_t e, rows, cols;   /* the shape                                            */
+    int32_t hb, wb;          /* ceil(rows/128), ceil(cols/128)                        */
+    int32_t bucket;          /* DP rank (shard) that owns the param's first block     */
+    int32_t reserved;        /* zero                                                  */
+} fp8z_param_entry;          /* 64 bytes */
+
+/* One DP shard: blocks [blk_begin, blk_begin + blk_count_real) carry data,
+ * [.. + blk_count_real, blk_begin + blk_capacity) are padding. */
+typedef struct { int64_t blk_begin, blk_count_real, blk_capacity; } fp8z_shard;
+
+/* One folded block: which param, expert index, block row/col; the valid
+ * rows/cols of a ragged edge block (128 inside).  param = -1 and valid = 0
+ * for a padding block. */
+typedef struct {
+    int32_t param, e, brow, bcol;
+    uint16_t valid_rows, valid_cols;
+} fp8z_block_desc;           /* 20 bytes */
+
+typedef struct {
+    int64_t real_elems;              /* sum of e*rows*cols                          */
+    int64_t total_blocks;            /* B: folded blocks holding data               */
+    int64_t fold_pad_elems;          /* zeros added by padding dims to 128          */
+    int64_t shard_pad_elems;         /* (capacity_blocks - B) * 16384               */
+    int64_t capacity_blocks;         /* blocks to allocate per state buffer          */
+    int64_t naive_straddled_blocks;  /* blocks an even split of the unfolded flat
+                                        buffer would cut across ranks                */
+} fp8z_plan_summary;
+
+/* AdamW + quantizer hyper-parameters.  The per-step scalars are formed on the
+ * host in double from these float values and rounded once to float:
+ * step_size = lr/(1-beta1^step), rs_bc2 = 1/sqrt(1-beta2^step),
+ * 1-beta1, 1-beta2, decay = 1-lr*weight_decay, lr*weight_decay. */
+typedef struct {
+    float lr, beta1, beta2, eps, weight_decay;
+    int64_t step;            /* >= 1                                          */
+    float fp8_max;           /* (0, 448]; 448 for E4M3                         */
+    float min_scale;         /* scale floor, >= 0 (1e-6 in the pages)          */
+    int32_t scale_mode;      /* fp8z_scale_mode                                */
+    int32_t decay_mode;      /* fp8z_decay_mode                                */
+} fp8z_adamw_hparams;        /* 48 bytes */
+
+/*
+ * fp8z_plan_shards -- host-only shard planner ("Param-wise split",
+ * "Block-wise split" of the ZeRO design page).
+ *
+ * shapes[nparams] (host) in model order; dp >= 1 shards.
+ * BLOCKWISE: every param is padded to multiples of 128 in rows and cols and
+ *   folded; params follow each other in the given order, blocks of a param in
+ *   (e, block row, block col) order.  With B blocks in all, each shard holds
+ *   C = ceil(B/dp) blocks: shard r = [r*C, min((r+1)*C, B)); the tail is padding.
+ * PARAMWISE: params sorted by padded block count (descending; ties keep model
+ *   order) go one by one to the least-loaded bucket (ties: lowest bucket);
+ *   every bucket is padded to the largest load `cap`; bucket r holds blocks
+ *   [r*cap, r*cap + load_r), its params in the order they were assigned.
+ * Outputs (host, caller-allocated): params_out[nparams], shards_out[dp],
+ * summary_out; blocks_out[capacity_blocks] descriptors, or NULL for a size
+ * query (summary_out->capacity_blocks tells how many to allocate).
+ * Returns FP8Z_OK, FP8Z_EINVAL (bad shape/dp/split/null), FP8Z_ENOSPACE
+ * (blocks_cap < capacity_blocks).  Deterministic; no device work.
+ */
+int fp8z_plan_shards(const fp8z_param_shape *shapes, int32_t nparams, int32_t dp,
+                     int32_t split, fp8z_param_entry *params_out, fp8z_shard *shards_out,
+                     fp8z_block_desc *blocks_out, int64_t blocks_cap,
+                     fp8z_plan_summary *summary_out);
+
+/*
+ * fp8z_adamw_requant_step -- the fused shard step ("Summary" steps: element-wise
+ * update of the rank's FP32 main params, then quantize the new FP8 weights and
+ * scales from them), for blocks [blk_begin, blk_begin + nblk).
+ *
+ * Per element, float32, each operation rounded on its own (no FMA):
+ *   m' = beta1*m + (1-beta1)*g;  v' = beta2*v + (1-beta2)*(g*g)
+ *   u  = m' / (sqrt(v')*rs_bc2 + eps)
+ *   PRE : p' = p*decay - step_size*u
+ *   POST: p1 = p - step_size*u;  p' = p1 - (lr*wd)*p1
+ * Per block: amax = max|p'|; EXACT: s = fp8_max/amax (FLT_MAX if infinite),
+ * s = max(s, min_scale), s = 1 when amax == 0; POW2: s = 2^floor(log2(fp8_max/
+ * amax)) floored at the smallest power of two >= min_scale; inv = 1/s;
+ * q = E4M3(p'*s), round to nearest even, saturated to ±448; NaN stays NaN.
+ *
+ * p, m, v (updated in place), g: device fp32 [capacity_blocks,128,128].
+ * w_fp8: device u8 [capacity_blocks,128,128]; inv_scale: device f32
+ *   [capacity_blocks].  Block b of every buffer is the same block.
+ * desc: device fp8z_block_desc[capacity_blocks] or NULL.  With desc, element
+ *   (r, c) of block b with r >= valid_rows or c >= valid_cols is padding: its
+ *   p', m', v' and q are written as 0 and it does not enter the amax.
+ * params / nparams: device fp8z_param_entry[nparams] (planner output), needed
+ *   only for the column-major copy.
+ * w_fp8_t / w_fp8_t_bytes, inv_scale_t / inv_scale_t_count: optional (both
+ *   NULL or both set; need desc and params).  For every data block, the
+ *   transposed 128x128 tile goes to the param's column-major copy
+ *   (w_fp8_t + t_offset + e*cols*rows, element [col][row], ld = rows) and inv
+ *   to inv_scale_t[t_scale_offset + e*wb*hb + bcol*hb + brow].  A block whose
+ *   destination falls outside the stated sizes is skipped and reported as
+ *   FP8Z_EINVAL in *dev_status.
+ * hp: host pointer.  dev_status: device int32 or NULL.
+ * Returns FP8Z_OK, FP8Z_EINVAL, FP8Z_EALIGN, FP8Z_ENOSPACE (blk_begin+nblk >
+ * capacity_blocks), FP8Z_EUNSUPPORTED, FP8Z_ECUDA.  nblk == 0 launches nothing.
+ */
+int fp8z_adamw_requant_step(float *p, const float *g, float *m, float *v,
+                            uint8_t *w_fp8, float *inv_scale, int64_t capacity_blocks,
+                            int64_t blk_begin, int64_t nblk,
+                            const fp8z_block_desc *desc,
+                            const fp8z_param_entry *params, int32_t nparams,
+                            uint8_t *w_fp8_t, int64_t w_fp8_t_bytes,
+                            float *inv_scale_t, int64_t inv_scale_t_count,
+                            const fp8z_adamw_hparams *hp, int32_t *dev_status,
+                            void *stream);
+
+/*
+ * fp8z_dequant -- out[b][i] = E4M3_value(w_fp8[b][i]) * inv_scale[b] (float
+ * product), for nblk blocks ("FP8-Flow-MoE" §3.1, D(Q(x)) = Q(x)*s).
+ * w_fp8: device u8 [nblk,128,128]; inv_scale: device f32 [nblk];
+ * out: device f32 [nblk,128,128].  Returns FP8Z_OK / EINVAL / EALIGN / ECUDA.
+ */
+int fp8z_dequant(const uint8_t *w_fp8, const float *inv_scale, int64_t nblk,
+                 float *out, void *stream);
+
+/*
+ * fp8z_transpose_fp8 -- column-major copy of one quantized param.  With
+ * 128x128 blocks one scale covers the whole 2-D block, so the layout change is
+ * an exact byte permutation and the scale grid is transposed: no dequantize /
+ * requantize round trip ("FP8-Flow-MoE" §3.1, scaling-aware transpose).
+ * w_fp8 / inv_scale: device, the folded flat buffers; the param's blocks start
+ *   at entry->blk_offset.
+ * entry: HOST pointer to the param's planner entry (shape, hb, wb, blk_offset).
+ * out: device u8 [e, cols, rows] (ld = rows); inv_scale_t: device f32
+ *   [e, wb, hb].  out must be 16-byte aligned; rows need not be a multiple of
+ *   16 (an unaligned row length takes a byte-store path).
+ * Returns FP8Z_OK / EINVAL / EALIGN / ECUDA.
+ */
+int fp8z_transpose_fp8(const uint8_t *w_fp8, const float *inv_scale,
+                       const fp8z_param_entry *entry, uint8_t *out, float *inv_scale_t,
+                       void *stream);
+
+/*
+ * fp8z_e4m3_encode_bits -- out[i] = E4M3 code (round to nearest even,
+ * saturating, as in the step) of the float whose bit pattern is
+ * first_bits + i, for i < n; n a multiple of 4, out device, 16-byte aligned.
+ * Exposes the step's float->E4M3 cast on its own so it can be checked over
+ * all 2^32 inputs ("FP8-Flow-MoE" §3.1 value formula).
+ */
+int fp8z_e4m3_encode_bits(uint32_t first_bits, int64_t n, uint8_t *out, void *stream);
+
+/*
+ * fp8z_watchdog_selftest -- launches one CTA that waits on a barrier nothing
+ * will complete, with the same bounded wait the step uses and a limit of
+ * timeout_ns nanoseconds; it then writes FP8Z_ETIMEOUT to *dev_status (device
+ * int32, starting at 0) and returns.  Lets a test see the device error path
+ * without any fault or hang.  timeout_ns in [0, 10^10].
+ */
+int fp8z_watchdog_selftest(int32_t *dev_status, int64_t timeout_ns, void *stream);
+
+/* Static string naming a status code (never NULL). */
+const char *fp8z_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP8Z_H */
