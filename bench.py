@@ -1,0 +1,485 @@
+#!/usr/bin/env python3
+"""Benchmark: fused AdamW + blockwise-E4M3 requant step on one GB300.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload flat6e9]
+
+Default workload: 117 tiles of 7168x7168 FP32 master params (6.01e9 elements,
+366,912 blocks of 128x128), step 1000, grads N(0,1e-4) with 0.1 % x100 spikes,
+column-major E4M3 copy with the transposed scale grid on.  One step = one pass
+of the whole hot path over the shard = one kernel launch.  The state (96 GB)
+is far larger than L2 (129 MB), so no L2 flush is needed between steps.
+
+Prints ONE JSON line on rank 0.  Under torchrun (N > 1) every rank runs its own
+replica on its own GPU (weak scaling, no collective on the data path); times
+are max-reduced across ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import hashlib
+import io
+import json
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "optimizer-step Gelem/s and achieved HBM GB/s (% of GB300 peak), 1 GPU"
+UNIT = "Gelem/s"
+FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 8000.0
+BLK = 16384
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "fp8z_step_kernel_flat6e9.md")
+KERNEL_SOURCES = ["blockwise_fp8_zero_gb300/csrc/step.cu", "blockwise_fp8_zero_gb300/csrc/fp8z_device.cuh"]
+
+
+# --------------------------------------------------------------------- env
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs, copy)"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback (6.8 TB/s, earlier GB300 measurement)"
+
+
+def kernel_hash():
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic():
+    """DRAM bytes per launch from the committed ncu summary, if the kernel
+    sources still hash to the ones profiled; else None."""
+    try:
+        txt = open(PROFILE_SUMMARY).read()
+    except OSError:
+        return None
+    vals = {}
+    for line in txt.splitlines():
+        if ":" in line and line.strip().startswith("- "):
+            k, v = line.strip()[2:].split(":", 1)
+            vals[k.strip()] = v.strip().strip("`")
+    if vals.get("kernel_sources_sha256") != kernel_hash():
+        return None
+    try:
+        return float(vals["dram_bytes_per_full_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi sampled every 200 ms while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid=None):
+        self.uuid = uuid
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(prefix="fp8z_clocks_", suffix=".csv")
+        os.close(fd)
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200"]
+        if self.uuid:
+            cmd.insert(1, f"--id={self.uuid}")
+        try:
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(cmd, stdout=self.out, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.out.close()
+
+    def summary(self):
+        if self.proc is None or not self.path:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = list(csv.reader(io.StringIO(open(self.path).read())))
+        os.unlink(self.path)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            r = [x.strip() for x in r]
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                smax.append(float(r[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, r[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": max(smax), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def host_mem_gb():
+    try:
+        for line in open("/proc/meminfo"):
+            if line.startswith("MemAvailable:"):
+                return int(line.split()[1]) / 1e6
+    except OSError:
+        pass
+    return 0.0
+
+
+# ----------------------------------------------------------- oracle (CPU)
+def cpu_oracle_run(w, host, hp_kw, threads):
+    """Time the oracle on host arrays (a block sample); returns seconds."""
+    import oracle
+    from concurrent.futures import ThreadPoolExecutor
+    ohp = oracle.Hparams.make(**hp_kw)
+    nb = host["p"].size // BLK
+    q = np.zeros(nb * BLK, np.uint8)
+    inv = np.zeros(nb, np.float32)
+    per = -(-nb // threads)
+
+    def run(b0):
+        b1 = min(nb, b0 + per)
+        sl = slice(b0 * BLK, b1 * BLK)
+        oracle.adamw_requant_step(host["p"][sl], host["g"][sl], host["m"][sl], host["v"][sl],
+                                  q[sl], inv[b0:b1], 0, b1 - b0, ohp)
+
+    t0 = time.perf_counter()
+    with ThreadPoolExecutor(threads) as ex:
+        list(ex.map(run, range(0, nb, per)))
+    return time.perf_counter() - t0
+
+
+def sample_host_blocks(w, nblocks, seed=0):
+    """The workload's distributions, drawn on the host for a block sample
+    (the sample is full 128x128 blocks of the same kind as the workload)."""
+    import torch
+    from blockwise_fp8_zero_gb300 import workloads
+    host = {}
+    for k in "pgmv":
+        t = torch.empty(nblocks * BLK, dtype=torch.float32)
+        workloads.fill(t, k, w.dists[k], seed + 17)
+        host[k] = t.numpy()
+    return host
+
+
+# --------------------------------------------------------------- our path
+def run_ours(args):
+    import torch
+    from blockwise_fp8_zero_gb300 import build, fp8z, workloads
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    build.build()
+    fp8z.lib()
+
+    w = workloads.get(args.workload)
+    free, total = torch.cuda.mem_get_info(dev)
+    per_elem = 16 + 1 + (1 if w.transposed else 0)
+    budget = int((free - (6 << 30)) / per_elem)
+    scaled_note = None
+    if w.real_elems > budget:
+        w = workloads.scaled(w, budget)
+        scaled_note = f"scaled to {w.real_elems} elements to fit {free / 1e9:.0f} GB free"
+
+    params, shards, blocks, summ = fp8z.fp8z_plan_shards(w.shapes, w.dp, w.split)
+    cap = int(summ["capacity_blocks"])
+    real = int(summ["real_elems"])
+    state = workloads.make_state(w, blocks, dev, seed=rank)
+    q = torch.empty(cap * BLK, dtype=torch.uint8, device=dev)
+    inv = torch.empty(cap, dtype=torch.float32, device=dev)
+    desc = fp8z.table_to_device(blocks, dev)
+    pdev = fp8z.table_to_device(params, dev)
+    t_bytes = int(sum(e * r * c for e, r, c in w.shapes))
+    t_scales = int(sum(int(p["e"]) * int(p["hb"]) * int(p["wb"]) for p in params))
+    wt = torch.empty(t_bytes, dtype=torch.uint8, device=dev) if w.transposed else None
+    it = torch.empty(t_scales, dtype=torch.float32, device=dev) if w.transposed else None
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.Stream(dev)
+    step0 = int(w.hp["step"])
+    hp_kw = dict(w.hp)
+
+    def one_step(t, s=stream):
+        hp = fp8z.hparams(**{**hp_kw, "step": t})
+        for sh in shards:      # one launch per shard; flat6e9 has a single shard
+            fp8z.fp8z_adamw_requant_step(state["p"], state["g"], state["m"], state["v"], q, inv,
+                                         int(sh["blk_begin"]), int(sh["blk_count_real"]), hp,
+                                         desc=desc, params=pdev if w.transposed else None,
+                                         nparams=len(params) if w.transposed else 0,
+                                         w_fp8_t=wt, inv_scale_t=it, dev_status=status, stream=s)
+
+    launches_per_step = len(shards)
+    t = step0
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            one_step(t)
+            t += 1
+    torch.cuda.synchronize(dev)
+    if status.item() != 0:
+        raise RuntimeError(fp8z.fp8z_status_string(status.item()))
+
+    def barrier():
+        if ws > 1:
+            import torch.distributed as dist
+            dist.barrier(device_ids=[local])
+
+    # ---- timed region: K steps, per-launch CUDA events on the launch stream
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    uuid = None
+    try:
+        uuid = str(torch.cuda.get_device_properties(dev).uuid)
+        if uuid and not uuid.startswith("GPU-"):
+            uuid = "GPU-" + uuid
+    except Exception:
+        uuid = None
+    with ClockSampler(uuid) as clocks:
+        barrier()
+        torch.cuda.synchronize(dev)
+        with torch.cuda.stream(stream):
+            ev[0].record(stream)
+            for i in range(args.steps):
+                one_step(t)
+                t += 1
+                ev[i + 1].record(stream)
+        torch.cuda.synchronize(dev)
+        barrier()
+    clk = clocks.summary()
+    if status.item() != 0:
+        raise RuntimeError(fp8z.fp8z_status_string(status.item()))
+    per_step_ms = [ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)]
+    total_ms = ev[0].elapsed_time(ev[-1])
+    if ws > 1:
+        import torch.distributed as dist
+        tt = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total_ms = float(tt.item())
+    value = real * args.steps * ws / (total_ms / 1e3) / 1e9
+
+    # algorithmic bytes per launch: read g, p, m, v; write p, m, v, codes
+    # (+ the column-major copy); plus per block a descriptor and inverse scale(s)
+    nblk_run = int(sum(int(s["blk_count_real"]) for s in shards))
+    per_block = BLK * (16 + 12 + 1 + (1 if w.transposed else 0)) + 20 + 4 + (4 if w.transposed else 0)
+    alg_bytes_step = nblk_run * per_block
+    avg_launch_s = (sum(per_step_ms) / len(per_step_ms)) / 1e3 / launches_per_step
+    achieved = alg_bytes_step / launches_per_step / avg_launch_s / 1e9
+    peak, peak_src = measured_peak()
+    traffic = profiled_traffic() if (scaled_note is None and launches_per_step == 1) else None
+
+    # ---- end to end through the C ABI with pinned host buffers
+    e2e = run_e2e(args, w, state, q, inv, wt, it, desc, pdev, params, shards, hp_kw, t, dev, ws)
+
+    line = {
+        "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": w.name, "params": len(w.shapes), "elements": real, "blocks": nblk_run,
+                   "dp_shards": w.dp, "column_major_copy": w.transposed, "step": step0,
+                   "l2": "state 96 GB >> 129 MB L2: no flush between steps",
+                   "launches_per_step": launches_per_step, "scaled": scaled_note,
+                   "hbm_gbs": round(achieved, 1),
+                   "frac_of_nominal_8tbs": round(achieved / NOMINAL_HBM_GBS, 4)},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "algorithmic_bytes": alg_bytes_step // launches_per_step,
+                     "peak_source": peak_src,
+                     "kernel": "fp8z_step_kernel", "kernel_ms": round(avg_launch_s * 1e3, 4)},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk,
+        "e2e": e2e,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, hp_kw, args)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def run_e2e(args, w, state, q, inv, wt, it, desc, pdev, params, shards, hp_kw, t, dev, ws):
+    """The same step end to end: every step copies the grads in from pinned host
+    memory and the E4M3 weights, inverse scales (and the column-major copy with
+    its scale grid) back out, pipelined over whole params/experts on three
+    streams (copy in, step, copy out).  The FP32 main params and moments stay
+    resident in HBM, as in ZeRO-1."""
+    import torch
+    from blockwise_fp8_zero_gb300 import fp8z
+    if len(shards) != 1:
+        return None
+    # whole-param units (experts of a 3-D bank) so the column-major copy of a
+    # unit is one contiguous range
+    units = []
+    for i, pe in enumerate(params):
+        nb_e = int(pe["hb"]) * int(pe["wb"])
+        for e in range(int(pe["e"])):
+            b0 = int(pe["blk_offset"]) + e * nb_e
+            t0 = int(pe["t_offset"]) + e * int(pe["rows"]) * int(pe["cols"])
+            s0 = int(pe["t_scale_offset"]) + e * nb_e
+            units.append((b0, nb_e, t0, int(pe["rows"]) * int(pe["cols"]), s0))
+    nunits = len(units)
+    per_unit_host = units[0][1] * BLK * 4 + units[0][1] * BLK * (2 if w.transposed else 1)
+    budget = max(1, int((host_mem_gb() * 1e9 * 0.5) // max(per_unit_host, 1)))
+    if budget < nunits:
+        units = units[:budget]
+    e_blocks = sum(u[1] for u in units)
+    b_end = units[-1][0] + units[-1][1]
+    g_host = torch.empty(b_end * BLK, dtype=torch.float32, pin_memory=True)
+    g_host.copy_(state["g"][: b_end * BLK])
+    q_host = torch.empty(b_end * BLK, dtype=torch.uint8, pin_memory=True)
+    inv_host = torch.empty(b_end, dtype=torch.float32, pin_memory=True)
+    t_end = units[-1][2] + units[-1][3] if w.transposed else 0
+    s_end = units[-1][4] + units[-1][1] if w.transposed else 0
+    wt_host = torch.empty(t_end, dtype=torch.uint8, pin_memory=True) if w.transposed else None
+    it_host = torch.empty(s_end, dtype=torch.float32, pin_memory=True) if w.transposed else None
+    s_in, s_run, s_out = (torch.cuda.Stream(dev) for _ in range(3))
+    steps = max(3, min(args.steps, 10))
+    h2d = e_blocks * BLK * 4
+    d2h = e_blocks * BLK + e_blocks * 4 + ((e_blocks * BLK + e_blocks * 4) if w.transposed else 0)
+
+    ran = [None] * len(units)      # kernel done with unit u (its g may be overwritten)
+    sent = [None] * len(units)     # outputs of unit u copied out (they may be overwritten)
+
+    def one(tstep):
+        hp = fp8z.hparams(**{**hp_kw, "step": tstep})
+        for u, (b0, nb, t0, tn, s0) in enumerate(units):
+            e_in, e_run, e_out = torch.cuda.Event(), torch.cuda.Event(), torch.cuda.Event()
+            if ran[u] is not None:
+                s_in.wait_event(ran[u])
+            with torch.cuda.stream(s_in):
+                state["g"][b0 * BLK:(b0 + nb) * BLK].copy_(g_host[b0 * BLK:(b0 + nb) * BLK], non_blocking=True)
+                e_in.record(s_in)
+            s_run.wait_event(e_in)
+            if sent[u] is not None:
+                s_run.wait_event(sent[u])
+            fp8z.fp8z_adamw_requant_step(state["p"], state["g"], state["m"], state["v"], q, inv, b0, nb, hp,
+                                         desc=desc, params=pdev if w.transposed else None,
+                                         nparams=len(params) if w.transposed else 0,
+                                         w_fp8_t=wt, inv_scale_t=it, stream=s_run)
+            e_run.record(s_run)
+            ran[u] = e_run
+            s_out.wait_event(e_run)
+            with torch.cuda.stream(s_out):
+                q_host[b0 * BLK:(b0 + nb) * BLK].copy_(q[b0 * BLK:(b0 + nb) * BLK], non_blocking=True)
+                inv_host[b0:b0 + nb].copy_(inv[b0:b0 + nb], non_blocking=True)
+                if w.transposed:
+                    wt_host[t0:t0 + tn].copy_(wt[t0:t0 + tn], non_blocking=True)
+                    it_host[s0:s0 + nb].copy_(it[s0:s0 + nb], non_blocking=True)
+                e_out.record(s_out)
+            sent[u] = e_out
+
+    one(t)
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    for i in range(steps):
+        one(t + 1 + i)
+    torch.cuda.synchronize(dev)
+    secs = time.perf_counter() - t0
+    if ws > 1:
+        import torch.distributed as dist
+        tt = torch.tensor([secs], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        secs = float(tt.item())
+    real = sum(u[3] for u in units)
+    return {"value": round(real * steps * ws / secs / 1e9, 4), "unit": UNIT,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
+            "units": f"{len(units)} of {nunits} tiles" if len(units) < nunits else f"all {nunits} tiles",
+            "note": "grads in, E4M3 weights + scales out per step; FP32 state resident"}
+
+
+def cpu_baseline(w, hp_kw, args, threads=None):
+    threads = threads or (os.cpu_count() or 1)
+    nblocks = args.cpu_blocks
+    host = sample_host_blocks(w, nblocks)
+    secs = cpu_oracle_run(w, host, {**hp_kw, "step": int(hp_kw["step"])}, threads)
+    return {"value": round(nblocks * BLK / secs / 1e9, 6), "unit": UNIT, "cores": threads,
+            "kind": "oracle",
+            "sample": f"{nblocks} full 128x128 blocks ({nblocks * BLK} elements) of the {w.name} "
+                      f"distributions, one oracle step, {threads} threads over block ranges, "
+                      f"{secs:.2f} s wall"}
+
+
+def run_reference(args):
+    ws, rank, local = dist_env()
+    if rank != 0:
+        return
+    from blockwise_fp8_zero_gb300 import workloads
+    import oracle
+    oracle.build_oracle()
+    w = workloads.get(args.workload)
+    threads = os.cpu_count() or 1
+    nblocks = args.cpu_blocks
+    host = sample_host_blocks(w, nblocks)
+    if args.warmup > 0:
+        cpu_oracle_run(w, {k: v.copy() for k, v in host.items()}, dict(w.hp), threads)
+    secs = 0.0
+    for i in range(args.steps):
+        secs += cpu_oracle_run(w, host, {**w.hp, "step": int(w.hp["step"]) + i}, threads)
+    value = nblocks * BLK * args.steps / secs / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": UNIT,
+            "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(secs / args.steps * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": w.name, "sample_blocks": nblocks,
+                       "note": "the CPU oracle on a block sample of the workload per step"},
+            "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": threads, "kind": "oracle",
+                             "sample": f"{nblocks} blocks of {w.name} per step"},
+            "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="flat6e9")
+    ap.add_argument("--cpu-blocks", type=int, default=12288)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

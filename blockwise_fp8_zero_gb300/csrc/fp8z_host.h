@@ -1,0 +1,40 @@
+// fp8z_host.h -- host-side helpers of the library (argument checks, device
+// queries, per-step AdamW scalars).  Internal; not part of the C ABI.
+#pragma once
+
+#include <cstdint>
+
+#include "fp8z.h"
+
+namespace fp8z {
+namespace host {
+
+// Limit for every bounded device wait (2 s): far above any legitimate wait in
+// a step, far below anything that would look like a hung GPU.
+constexpr int64_t kDefaultTimeoutNs = 2000000000LL;
+
+inline bool aligned(const void* ptr, uintptr_t a) {
+    return (reinterpret_cast<uintptr_t>(ptr) & (a - 1)) == 0;
+}
+
+// Scalars of one AdamW step, formed in double from the float hyper-parameters
+// and rounded once to float.
+struct AdamwScalars {
+    float beta1, beta2, omb1, omb2, eps, step_size, rs_bc2, decay, lr_wd;
+};
+
+AdamwScalars adamw_scalars(const fp8z_adamw_hparams& hp);
+bool hparams_valid(const fp8z_adamw_hparams& hp);
+
+// Smallest power of two >= x (x > 0, finite); 0 for x == 0.
+float pow2_at_least(float x);
+
+// SM count of the current device; FP8Z_EUNSUPPORTED unless it is an sm_103
+// part (the library is built for sm_103a only).
+int device_sms(int* sms);
+
+// cudaFuncSetAttribute(MaxDynamicSharedMemorySize) once per (kernel slot, device).
+int set_smem_once(const void* kernel, int slot, int bytes);
+
+}  // namespace host
+}  // namespace fp8z

@@ -1,0 +1,430 @@
+// step.cu -- fused AdamW + blockwise-E4M3 requantization of one DP shard
+// (sm_103a).
+//
+// Method: "A ZeRO Optimizer Design for Blockwise FP8 Quantization", "Summary":
+// each DP rank updates its folded FP32 main-param shard element-wise, then
+// quantizes the new FP8 weights and per-block scales from those FP32 values.
+// Update as printed in the lpnh.cn "Model-Optimizer" article §4.3; scale
+// 448/amax with the 1e-6 floor of mhpn.cn "Core scaling strategies in FP8
+// training" §3.2/§4.2; nearest-value E4M3 rounding of "FP8-Flow-MoE" §3.1.
+//
+// Design (GB300): a persistent kernel, one CTA per SM.  One producer warp
+// streams each 128x128 block's g, p, m, v through a ring of shared-memory
+// stages with the TMA bulk-copy engine (16 rows x 128 = 2048 floats per
+// tensor per stage), so ~200 KB per SM are in flight independent of register
+// pressure.  Sixteen consumer warps apply AdamW in registers, stream p', m', v'
+// straight back to HBM and keep p' (32 values per thread) until the block's
+// amax is known; the amax comes from warp shuffles plus one shared-memory
+// exchange, then the same registers are cast to E4M3.  HBM traffic is the
+// algorithmic 16 B read + 13 B written per element (+1 B for the optional
+// column-major copy).  The producer keeps loading the next block while the
+// consumers reduce and quantize, so the memory pipe never drains.  Every wait
+// is bounded (fp8z_device.cuh); no tensor cores: the op is element-wise.
+#include <cfloat>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+
+#include <cuda_runtime.h>
+
+#include "fp8z.h"
+#include "fp8z_device.cuh"
+#include "fp8z_host.h"
+
+namespace fp8z {
+namespace {
+
+constexpr int kBlk = FP8Z_BLOCK;
+constexpr int kBlkElems = FP8Z_BLOCK_ELEMS;
+constexpr int kConsumerWarps = 16;
+constexpr int kConsumers = kConsumerWarps * 32;
+constexpr int kThreads = kConsumers + 32;               // + one producer warp
+constexpr int kStageRows = kConsumerWarps;              // one row per consumer warp
+constexpr int kStageElems = kStageRows * kBlk;          // 2048
+constexpr int kStagesPerBlock = kBlk / kStageRows;      // 8
+constexpr uint32_t kTensorStageBytes = kStageElems * 4; // 8 KB
+constexpr uint32_t kStageBytes = 4 * kTensorStageBytes; // g, p, m, v: 32 KB
+constexpr int kRing = 6;                                // 192 KB of stages
+
+constexpr size_t kRingBytes = size_t(kRing) * kStageBytes;
+constexpr size_t kTileBytes = kBlkElems;                 // 16 KB byte tile
+constexpr size_t kAmaxBytes = 2 * kConsumerWarps * sizeof(float);
+constexpr size_t kBarOffset = kRingBytes + kTileBytes + kAmaxBytes;
+constexpr int kNumBars = 2 * kRing + 2;
+constexpr size_t kSmemBytes = kBarOffset + kNumBars * 8 + 16;
+
+struct StepArgs {
+    float* p;
+    const float* g;
+    float* m;
+    float* v;
+    uint8_t* w_fp8;
+    float* inv_scale;
+    int64_t blk_begin, nblk;
+    const fp8z_block_desc* desc;
+    const fp8z_param_entry* params;
+    int32_t nparams;
+    uint8_t* w_fp8_t;
+    int64_t w_fp8_t_bytes;
+    float* inv_scale_t;
+    int64_t inv_scale_t_count;
+    int32_t* dev_status;
+    int64_t timeout_ns;
+    float beta1, beta2, omb1, omb2, eps, step_size, rs_bc2, decay, lr_wd;
+    float fp8_max, min_scale, min_scale_pow2;
+    int32_t scale_mode, decay_mode;
+};
+
+// AdamW on one element, float32, one rounding per operation, never fused.
+__device__ __forceinline__ void adamw1(const StepArgs& A, float p, float g, float m, float v,
+                                       float& p1, float& m1, float& v1) {
+    m1 = __fadd_rn(__fmul_rn(A.beta1, m), __fmul_rn(A.omb1, g));
+    v1 = __fadd_rn(__fmul_rn(A.beta2, v), __fmul_rn(A.omb2, __fmul_rn(g, g)));
+    const float d = __fadd_rn(__fmul_rn(__fsqrt_rn(v1), A.rs_bc2), A.eps);
+    const float su = __fmul_rn(A.step_size, __fdiv_rn(m1, d));
+    if (A.decay_mode == FP8Z_DECAY_PRE) {
+        p1 = __fsub_rn(__fmul_rn(p, A.decay), su);
+    } else {
+        const float pu = __fsub_rn(p, su);
+        p1 = __fsub_rn(pu, __fmul_rn(A.lr_wd, pu));
+    }
+}
+
+// Largest power of two s with s * amax <= fp8_max (amax > 0, finite), from
+// the exponent and significand bits.
+__device__ __forceinline__ float pow2_scale(float amax, float fp8_max) {
+    auto split = [](float x, int& e, uint32_t& sig) {
+        uint32_t b = __float_as_uint(x);
+        uint32_t ex = b >> 23, man = b & 0x7FFFFFu;
+        if (ex == 0) {                       // subnormal: normalise
+            int msb = 31 - __clz(man);       // 0..22
+            e = msb - 149;
+            sig = (man << (23 - msb)) & 0x7FFFFFu;
+        } else {
+            e = int(ex) - 127;
+            sig = man;
+        }
+    };
+    int ea, em;
+    uint32_t sa, sm;
+    split(amax, ea, sa);
+    split(fp8_max, em, sm);
+    int k = em - ea - (sa > sm ? 1 : 0);
+    if (k > 127) k = 127;
+    if (k < -126) return 0.0f;               // amax >= 2^127 * 448: cannot happen for finite amax
+    return __uint_as_float(uint32_t(k + 127) << 23);
+}
+
+__device__ __forceinline__ float block_scale(const StepArgs& A, float amax) {
+    if (amax == 0.0f) return 1.0f;
+    float s;
+    if (A.scale_mode == FP8Z_SCALE_EXACT) {
+        s = __fdiv_rn(A.fp8_max, amax);
+        if (s > FLT_MAX) s = FLT_MAX;
+        s = fmaxf(s, A.min_scale);
+    } else {
+        s = (amax > FLT_MAX) ? 0.0f : pow2_scale(amax, A.fp8_max);
+        s = fmaxf(s, A.min_scale_pow2);
+    }
+    return s;
+}
+
+__device__ __forceinline__ int64_t imin64(int64_t a, int64_t b) { return a < b ? a : b; }
+
+__device__ __forceinline__ float4 lds4(const float* p) {
+    return *reinterpret_cast<const float4*>(p);
+}
+
+__device__ __forceinline__ float absmax4(float acc, float4 x) {
+    return fmaxf(fmaxf(fmaxf(acc, fabsf(x.x)), fmaxf(fabsf(x.y), fabsf(x.z))), fabsf(x.w));
+}
+
+struct BlockInfo {
+    int vr, vc;          // valid rows / cols
+    int param, e, brow, bcol;
+};
+
+__device__ __forceinline__ BlockInfo load_desc(const StepArgs& A, int64_t blk) {
+    BlockInfo bi{kBlk, kBlk, -1, 0, 0, 0};
+    if (A.desc) {
+        const int* d = reinterpret_cast<const int*>(A.desc + blk);
+        bi.param = __ldg(d + 0);
+        bi.e = __ldg(d + 1);
+        bi.brow = __ldg(d + 2);
+        bi.bcol = __ldg(d + 3);
+        const uint32_t valid = static_cast<uint32_t>(__ldg(d + 4));
+        bi.vr = int(valid & 0xFFFFu);
+        bi.vc = int(valid >> 16);
+    }
+    return bi;
+}
+
+__global__ void __launch_bounds__(kThreads, 1) fp8z_step_kernel(const StepArgs A) {
+    extern __shared__ __align__(1024) unsigned char smem[];
+    float* ring = reinterpret_cast<float*>(smem);
+    uint32_t* tile = reinterpret_cast<uint32_t*>(smem + kRingBytes);
+    float* amax_x = reinterpret_cast<float*>(smem + kRingBytes + kTileBytes);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kBarOffset);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + kNumBars);
+
+    const uint32_t full0 = smem_addr(bars);
+    const uint32_t empty0 = smem_addr(bars + kRing);
+    const uint32_t amax_bar = smem_addr(bars + 2 * kRing);
+    const uint32_t tile_bar = smem_addr(bars + 2 * kRing + 1);
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
+
+    if (tid == 0) {
+        for (int s = 0; s < kRing; ++s) {
+            mbar_init(full0 + 8 * s, 1);
+            mbar_init(empty0 + 8 * s, kConsumerWarps);
+        }
+        mbar_init(amax_bar, kConsumerWarps);
+        mbar_init(tile_bar, kConsumerWarps);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    const Watchdog wd{abort_flag, A.dev_status, A.timeout_ns};
+    // grid <= nblk, so every CTA owns at least one block
+    const int64_t nmine = (A.nblk - blockIdx.x + gridDim.x - 1) / gridDim.x;
+
+    if (warp == kConsumerWarps) {
+        // ------------------------------------------------------ producer
+        if (lane != 0) return;
+        const uint64_t pol = l2_evict_first_policy();
+        const uint32_t ring0 = smem_addr(ring);
+        int slot = 0;
+        uint32_t phase = 0;
+        int64_t issued = 0;
+        for (int64_t i = 0; i < nmine; ++i) {
+            const int64_t blk = A.blk_begin + blockIdx.x + i * gridDim.x;
+            const size_t base = size_t(blk) * kBlkElems;
+            for (int k = 0; k < kStagesPerBlock; ++k) {
+                if (!mbar_wait_bounded(empty0 + 8 * slot, phase ^ 1, wd)) goto drain;
+                const uint32_t full = full0 + 8 * slot;
+                mbar_arrive_expect_tx(full, kStageBytes);
+                const uint32_t dst = ring0 + slot * kStageBytes;
+                const size_t off = base + size_t(k) * kStageElems;
+                bulk_g2s(dst + 0 * kTensorStageBytes, A.g + off, kTensorStageBytes, full, pol);
+                bulk_g2s(dst + 1 * kTensorStageBytes, A.p + off, kTensorStageBytes, full, pol);
+                bulk_g2s(dst + 2 * kTensorStageBytes, A.m + off, kTensorStageBytes, full, pol);
+                bulk_g2s(dst + 3 * kTensorStageBytes, A.v + off, kTensorStageBytes, full, pol);
+                ++issued;
+                if (++slot == kRing) { slot = 0; phase ^= 1; }
+            }
+        }
+        return;
+    drain:
+        // Abort: let the copies already issued land before the CTA exits.
+        for (int64_t j = (issued > kRing ? issued - kRing : 0); j < issued; ++j) {
+            const int s = int(j % kRing);
+            const uint32_t ph = uint32_t((j / kRing) & 1);
+            mbar_wait_bounded(full0 + 8 * s, ph, wd, /*honor_abort=*/false);
+        }
+        return;
+    }
+
+    // ---------------------------------------------------------- consumers
+    const int col = lane * 4;
+    const bool transposed = (A.w_fp8_t != nullptr);
+    int slot = 0;
+    uint32_t phase = 0;
+    uint32_t tile_phase = 0;
+
+    for (int64_t i = 0; i < nmine; ++i) {
+        const int64_t blk = A.blk_begin + blockIdx.x + i * gridDim.x;
+        const size_t base = size_t(blk) * kBlkElems;
+        const BlockInfo bi = load_desc(A, blk);
+
+        float4 keep[kStagesPerBlock];
+        float lmax = 0.0f;
+#pragma unroll
+        for (int k = 0; k < kStagesPerBlock; ++k) {
+            if (!mbar_wait_bounded(full0 + 8 * slot, phase, wd)) return;
+            const float* st = ring + size_t(slot) * (kStageBytes / 4);
+            const float4 g4 = lds4(st + 0 * kStageElems + tid * 4);
+            const float4 p4 = lds4(st + 1 * kStageElems + tid * 4);
+            const float4 m4 = lds4(st + 2 * kStageElems + tid * 4);
+            const float4 v4 = lds4(st + 3 * kStageElems + tid * 4);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty0 + 8 * slot);
+            if (++slot == kRing) { slot = 0; phase ^= 1; }
+
+            float4 p1, m1, v1;
+            adamw1(A, p4.x, g4.x, m4.x, v4.x, p1.x, m1.x, v1.x);
+            adamw1(A, p4.y, g4.y, m4.y, v4.y, p1.y, m1.y, v1.y);
+            adamw1(A, p4.z, g4.z, m4.z, v4.z, p1.z, m1.z, v1.z);
+            adamw1(A, p4.w, g4.w, m4.w, v4.w, p1.w, m1.w, v1.w);
+
+            const int row = k * kStageRows + warp;
+            if (row >= bi.vr || col + 3 >= bi.vc) {     // padding of a ragged edge block
+                const bool rv = row < bi.vr;
+                if (!(rv && col + 0 < bi.vc)) { p1.x = 0.f; m1.x = 0.f; v1.x = 0.f; }
+                if (!(rv && col + 1 < bi.vc)) { p1.y = 0.f; m1.y = 0.f; v1.y = 0.f; }
+                if (!(rv && col + 2 < bi.vc)) { p1.z = 0.f; m1.z = 0.f; v1.z = 0.f; }
+                if (!(rv && col + 3 < bi.vc)) { p1.w = 0.f; m1.w = 0.f; v1.w = 0.f; }
+            }
+            const size_t off = base + size_t(row) * kBlk + col;
+            *reinterpret_cast<float4*>(A.p + off) = p1;
+            *reinterpret_cast<float4*>(A.m + off) = m1;
+            *reinterpret_cast<float4*>(A.v + off) = v1;
+            keep[k] = p1;
+            lmax = absmax4(lmax, p1);
+        }
+
+        // ---- block amax: warp shuffle, then one exchange through shared memory
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) lmax = fmaxf(lmax, __shfl_xor_sync(0xFFFFFFFFu, lmax, o));
+        float* ax = amax_x + (i & 1) * kConsumerWarps;
+        if (lane == 0) {
+            ax[warp] = lmax;
+            mbar_arrive(amax_bar);
+        }
+        if (!mbar_wait_bounded(amax_bar, uint32_t(i & 1), wd)) return;
+        float amax = ax[0];
+#pragma unroll
+        for (int w = 1; w < kConsumerWarps; ++w) amax = fmaxf(amax, ax[w]);
+
+        const float s = block_scale(A, amax);
+        const float inv = __fdiv_rn(1.0f, s);
+        if (tid == 0) A.inv_scale[blk] = inv;
+
+        // ---- quantize the kept p' and store the row-major E4M3 block
+        uint32_t words[kStagesPerBlock];
+#pragma unroll
+        for (int k = 0; k < kStagesPerBlock; ++k) {
+            const float4 x = keep[k];
+            words[k] = pack_e4m3x4(__fmul_rn(x.x, s), __fmul_rn(x.y, s), __fmul_rn(x.z, s),
+                                   __fmul_rn(x.w, s));
+            const int row = k * kStageRows + warp;
+            *reinterpret_cast<uint32_t*>(A.w_fp8 + base + size_t(row) * kBlk + col) = words[k];
+        }
+
+        // ---- optional column-major copy of the param + transposed scale grid
+        if (!transposed || bi.param < 0) continue;
+        bool ok = bi.param < A.nparams;
+        int64_t H = 0, W = 0, t_base = 0, s_idx = 0;
+        if (ok) {
+            const fp8z_param_entry* pe = A.params + bi.param;
+            const int64_t pe_e = __ldg(&pe->e);
+            H = __ldg(&pe->rows);
+            W = __ldg(&pe->cols);
+            const int64_t hb = __ldg(&pe->hb), wb = __ldg(&pe->wb);
+            const int64_t t_off = __ldg(&pe->t_offset), ts_off = __ldg(&pe->t_scale_offset);
+            ok = bi.e >= 0 && bi.e < pe_e && bi.brow >= 0 && bi.brow < hb && bi.bcol >= 0 &&
+                 bi.bcol < wb && bi.vr == imin64(kBlk, H - bi.brow * int64_t(kBlk)) &&
+                 bi.vc == imin64(kBlk, W - bi.bcol * int64_t(kBlk)) && t_off >= 0 &&
+                 ts_off >= 0 && t_off + (bi.e + 1) * H * W <= A.w_fp8_t_bytes &&
+                 ts_off + (bi.e + 1) * hb * wb <= A.inv_scale_t_count;
+            t_base = t_off + bi.e * H * W;
+            s_idx = ts_off + bi.e * wb * hb + bi.bcol * hb + bi.brow;
+        }
+        if (!ok) {
+            if (tid == 0) report_status(A.dev_status, FP8Z_EINVAL);
+            continue;
+        }
+#pragma unroll
+        for (int k = 0; k < kStagesPerBlock; ++k) {
+            const int row = k * kStageRows + warp;
+            tile[row * 32 + (lane ^ tile_swz(row))] = words[k];
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(tile_bar);
+        if (!mbar_wait_bounded(tile_bar, tile_phase, wd)) return;
+        tile_phase ^= 1;
+
+        if (tid == 0) A.inv_scale_t[s_idx] = inv;
+        const bool aligned = ((t_base | H) & 3) == 0;
+        const int r0 = lane * 4;                       // input rows r0..r0+3
+        uint8_t* out_blk = A.w_fp8_t + t_base + bi.brow * int64_t(kBlk);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int cg = warp + h * kConsumerWarps;  // input cols 4cg..4cg+3
+            uint32_t w4[4];
+#pragma unroll
+            for (int ii = 0; ii < 4; ++ii) w4[ii] = tile[(r0 + ii) * 32 + (cg ^ tile_swz(r0 + ii))];
+            uint32_t o[4];
+            transpose4x4(w4[0], w4[1], w4[2], w4[3], o[0], o[1], o[2], o[3]);
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) {
+                const int c = 4 * cg + cc;
+                if (c >= bi.vc || r0 >= bi.vr) continue;
+                uint8_t* dst = out_blk + (bi.bcol * int64_t(kBlk) + c) * H + r0;
+                if (aligned && r0 + 3 < bi.vr) {
+                    *reinterpret_cast<uint32_t*>(dst) = o[cc];
+                } else {
+                    for (int b = 0; b < 4 && r0 + b < bi.vr; ++b) dst[b] = uint8_t(o[cc] >> (8 * b));
+                }
+            }
+        }
+    }
+}
+
+}  // namespace
+}  // namespace fp8z
+
+using namespace fp8z;
+
+extern "C" int fp8z_adamw_requant_step(float* p, const float* g, float* m, float* v,
+                                       uint8_t* w_fp8, float* inv_scale, int64_t capacity_blocks,
+                                       int64_t blk_begin, int64_t nblk,
+                                       const fp8z_block_desc* desc,
+                                       const fp8z_param_entry* params, int32_t nparams,
+                                       uint8_t* w_fp8_t, int64_t w_fp8_t_bytes,
+                                       float* inv_scale_t, int64_t inv_scale_t_count,
+                                       const fp8z_adamw_hparams* hp, int32_t* dev_status,
+                                       void* stream) {
+    if (!p || !g || !m || !v || !w_fp8 || !inv_scale || !hp) return FP8Z_EINVAL;
+    if (capacity_blocks < 0 || blk_begin < 0 || nblk < 0) return FP8Z_EINVAL;
+    if (capacity_blocks > (INT64_MAX / kBlkElems) / 4) return FP8Z_EINVAL;
+    if (blk_begin > capacity_blocks || nblk > capacity_blocks - blk_begin) return FP8Z_ENOSPACE;
+    const bool want_t = (w_fp8_t != nullptr) || (inv_scale_t != nullptr);
+    if (want_t && (!w_fp8_t || !inv_scale_t || !desc || !params || nparams <= 0 ||
+                   w_fp8_t_bytes < 0 || inv_scale_t_count < 0))
+        return FP8Z_EINVAL;
+    if (!host::aligned(p, 16) || !host::aligned(g, 16) || !host::aligned(m, 16) ||
+        !host::aligned(v, 16) || !host::aligned(w_fp8, 16) || !host::aligned(inv_scale, 4) ||
+        !host::aligned(desc, 4) || !host::aligned(params, 8) || !host::aligned(w_fp8_t, 16) ||
+        !host::aligned(inv_scale_t, 4) || !host::aligned(dev_status, 4))
+        return FP8Z_EALIGN;
+    if (!host::hparams_valid(*hp)) return FP8Z_EINVAL;
+    if (nblk == 0) return FP8Z_OK;
+
+    int sms = 0;
+    int rc = host::device_sms(&sms);
+    if (rc != FP8Z_OK) return rc;
+    static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+    rc = host::set_smem_once(reinterpret_cast<const void*>(&fp8z_step_kernel), 0, int(kSmemBytes));
+    if (rc != FP8Z_OK) return rc;
+
+    StepArgs A;
+    std::memset(&A, 0, sizeof(A));
+    A.p = p; A.g = g; A.m = m; A.v = v;
+    A.w_fp8 = w_fp8; A.inv_scale = inv_scale;
+    A.blk_begin = blk_begin; A.nblk = nblk;
+    A.desc = desc;
+    A.params = want_t ? params : nullptr;
+    A.nparams = nparams;
+    A.w_fp8_t = want_t ? w_fp8_t : nullptr;
+    A.w_fp8_t_bytes = w_fp8_t_bytes;
+    A.inv_scale_t = want_t ? inv_scale_t : nullptr;
+    A.inv_scale_t_count = inv_scale_t_count;
+    A.dev_status = dev_status;
+    A.timeout_ns = host::kDefaultTimeoutNs;
+    host::AdamwScalars sc = host::adamw_scalars(*hp);
+    A.beta1 = sc.beta1; A.beta2 = sc.beta2; A.omb1 = sc.omb1; A.omb2 = sc.omb2;
+    A.eps = sc.eps; A.step_size = sc.step_size; A.rs_bc2 = sc.rs_bc2;
+    A.decay = sc.decay; A.lr_wd = sc.lr_wd;
+    A.fp8_max = hp->fp8_max; A.min_scale = hp->min_scale;
+    A.min_scale_pow2 = host::pow2_at_least(hp->min_scale);
+    A.scale_mode = hp->scale_mode; A.decay_mode = hp->decay_mode;
+
+    const int64_t grid = nblk < sms ? nblk : sms;
+    fp8z_step_kernel<<<dim3(unsigned(grid)), dim3(kThreads), kSmemBytes,
+                       static_cast<cudaStream_t>(stream)>>>(A);
+    return cudaGetLastError() == cudaSuccess ? FP8Z_OK : FP8Z_ECUDA;
+}

@@ -1,0 +1,239 @@
+"""Thin ctypes binding of libfp8z.so (include/fp8z.h), same names as the C ABI.
+
+Argument marshalling only: every step of the optimizer path runs in the CUDA
+kernels of libfp8z.so.  Device buffers are torch CUDA tensors (PyTorch is used
+for device memory and streams); planner tables are numpy arrays.  A non-zero
+status raises Fp8zError.  There is no fallback: if the library is missing or
+was not built, loading fails loudly.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libfp8z.so")
+
+BLOCK = 128
+BLOCK_ELEMS = BLOCK * BLOCK
+
+FP8Z_OK, FP8Z_EINVAL, FP8Z_EALIGN, FP8Z_ENOSPACE = 0, -1, -2, -3
+FP8Z_ECUDA, FP8Z_ETIMEOUT, FP8Z_EUNSUPPORTED = -4, -5, -6
+FP8Z_SPLIT_BLOCKWISE, FP8Z_SPLIT_PARAMWISE = 0, 1
+FP8Z_SCALE_EXACT, FP8Z_SCALE_POW2 = 0, 1
+FP8Z_DECAY_PRE, FP8Z_DECAY_POST = 0, 1
+
+# numpy views of the ABI structs (include/fp8z.h)
+param_shape_dtype = np.dtype([("e", "<i8"), ("rows", "<i8"), ("cols", "<i8")])
+param_entry_dtype = np.dtype([
+    ("blk_offset", "<i8"), ("t_offset", "<i8"), ("t_scale_offset", "<i8"),
+    ("e", "<i8"), ("rows", "<i8"), ("cols", "<i8"),
+    ("hb", "<i4"), ("wb", "<i4"), ("bucket", "<i4"), ("reserved", "<i4"),
+])
+shard_dtype = np.dtype([("blk_begin", "<i8"), ("blk_count_real", "<i8"), ("blk_capacity", "<i8")])
+block_desc_dtype = np.dtype([
+    ("param", "<i4"), ("e", "<i4"), ("brow", "<i4"), ("bcol", "<i4"),
+    ("valid_rows", "<u2"), ("valid_cols", "<u2"),
+])
+plan_summary_dtype = np.dtype([
+    ("real_elems", "<i8"), ("total_blocks", "<i8"), ("fold_pad_elems", "<i8"),
+    ("shard_pad_elems", "<i8"), ("capacity_blocks", "<i8"), ("naive_straddled_blocks", "<i8"),
+])
+assert param_entry_dtype.itemsize == 64 and block_desc_dtype.itemsize == 20
+
+EXPORTED = ("fp8z_plan_shards", "fp8z_adamw_requant_step", "fp8z_dequant",
+            "fp8z_transpose_fp8", "fp8z_e4m3_encode_bits", "fp8z_watchdog_selftest",
+            "fp8z_status_string")
+
+
+class fp8z_adamw_hparams(ctypes.Structure):
+    _fields_ = [
+        ("lr", ctypes.c_float), ("beta1", ctypes.c_float), ("beta2", ctypes.c_float),
+        ("eps", ctypes.c_float), ("weight_decay", ctypes.c_float), ("step", ctypes.c_int64),
+        ("fp8_max", ctypes.c_float), ("min_scale", ctypes.c_float),
+        ("scale_mode", ctypes.c_int32), ("decay_mode", ctypes.c_int32),
+    ]
+
+
+assert ctypes.sizeof(fp8z_adamw_hparams) == 48
+
+
+def hparams(lr=1e-4, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1, step=1,
+            fp8_max=448.0, min_scale=1e-6, scale_mode=FP8Z_SCALE_EXACT,
+            decay_mode=FP8Z_DECAY_PRE) -> fp8z_adamw_hparams:
+    return fp8z_adamw_hparams(lr, beta1, beta2, eps, weight_decay, step, fp8_max, min_scale,
+                              scale_mode, decay_mode)
+
+
+class Fp8zError(RuntimeError):
+    def __init__(self, fn, status):
+        self.status = status
+        super().__init__(f"{fn}: {fp8z_status_string(status)} ({status})")
+
+
+_lib = None
+
+
+def lib():
+    """Load libfp8z.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(f"{LIB_PATH} is missing: build it with "
+                              "`python -c 'import __graft_entry__ as g; g.build()'`")
+        L = ctypes.CDLL(LIB_PATH)
+        P, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32
+        L.fp8z_plan_shards.argtypes = [P, i32, i32, i32, P, P, P, i64, P]
+        L.fp8z_adamw_requant_step.argtypes = [P, P, P, P, P, P, i64, i64, i64, P, P, i32,
+                                              P, i64, P, i64,
+                                              ctypes.POINTER(fp8z_adamw_hparams), P, P]
+        L.fp8z_dequant.argtypes = [P, P, i64, P, P]
+        L.fp8z_transpose_fp8.argtypes = [P, P, P, P, P, P]
+        L.fp8z_e4m3_encode_bits.argtypes = [ctypes.c_uint32, i64, P, P]
+        L.fp8z_watchdog_selftest.argtypes = [P, i64, P]
+        L.fp8z_status_string.argtypes = [ctypes.c_int]
+        L.fp8z_status_string.restype = ctypes.c_char_p
+        for name in EXPORTED:
+            if name != "fp8z_status_string":
+                getattr(L, name).restype = ctypes.c_int
+        _lib = L
+    return _lib
+
+
+def fp8z_status_string(status: int) -> str:
+    return lib().fp8z_status_string(int(status)).decode()
+
+
+def _check(fn, rc):
+    if rc != FP8Z_OK:
+        raise Fp8zError(fn, rc)
+
+
+def _dptr(t, dtype=None, name="tensor"):
+    """Device pointer of a contiguous CUDA tensor (None -> NULL)."""
+    if t is None:
+        return None
+    if not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    return t.data_ptr()
+
+
+def _stream_handle(stream):
+    import torch
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+# ---------------------------------------------------------------- planner
+def fp8z_plan_shards(shapes, dp, split=FP8Z_SPLIT_BLOCKWISE, with_blocks=True):
+    """shapes: iterable of (e, rows, cols).  Returns (params, shards, blocks, summary)
+    as numpy structured arrays (blocks None when with_blocks is False)."""
+    sh = np.array([tuple(int(x) for x in s) for s in shapes], dtype=param_shape_dtype)
+    n = len(sh)
+    params = np.zeros(max(n, 1), dtype=param_entry_dtype)
+    shards = np.zeros(max(int(dp), 1), dtype=shard_dtype)
+    summ = np.zeros(1, dtype=plan_summary_dtype)
+    L = lib()
+    rc = L.fp8z_plan_shards(sh.ctypes.data if n else None, n, int(dp), int(split),
+                            params.ctypes.data, shards.ctypes.data, None, 0, summ.ctypes.data)
+    _check("fp8z_plan_shards", rc)
+    blocks = None
+    if with_blocks:
+        cap = int(summ["capacity_blocks"][0])
+        blocks = np.zeros(max(cap, 1), dtype=block_desc_dtype)
+        rc = L.fp8z_plan_shards(sh.ctypes.data if n else None, n, int(dp), int(split),
+                                params.ctypes.data, shards.ctypes.data, blocks.ctypes.data,
+                                cap, summ.ctypes.data)
+        _check("fp8z_plan_shards", rc)
+        blocks = blocks[:cap]
+    return params[:n], shards[:int(dp)], blocks, summ[0]
+
+
+def table_to_device(arr, device="cuda"):
+    """Copy a planner table (numpy structured array) into a CUDA byte tensor."""
+    import torch
+    raw = np.ascontiguousarray(arr).view(np.uint8).reshape(-1)
+    return torch.from_numpy(raw.copy()).to(device)
+
+
+# ------------------------------------------------------------------ device
+def fp8z_adamw_requant_step(p, g, m, v, w_fp8, inv_scale, blk_begin, nblk, hp,
+                            desc=None, params=None, nparams=0, w_fp8_t=None,
+                            inv_scale_t=None, dev_status=None, stream=None):
+    """Fused AdamW + blockwise E4M3 requant of blocks [blk_begin, blk_begin+nblk).
+
+    p, g, m, v: float32 CUDA tensors of capacity*16384 elements; w_fp8 uint8 of
+    the same count; inv_scale float32 [capacity]; desc / params: CUDA byte
+    tensors from table_to_device (or None); w_fp8_t uint8, inv_scale_t float32
+    (optional column-major copy); dev_status int32 CUDA tensor (or None).
+    """
+    import torch
+    cap = p.numel() // BLOCK_ELEMS
+    for t, name in ((g, "g"), (m, "m"), (v, "v"), (w_fp8, "w_fp8")):
+        if t.numel() != p.numel():
+            raise ValueError(f"{name} must have as many elements as p")
+    if inv_scale.numel() < cap:
+        raise ValueError("inv_scale must hold one scale per block")
+    rc = lib().fp8z_adamw_requant_step(
+        _dptr(p, torch.float32, "p"), _dptr(g, torch.float32, "g"),
+        _dptr(m, torch.float32, "m"), _dptr(v, torch.float32, "v"),
+        _dptr(w_fp8, torch.uint8, "w_fp8"), _dptr(inv_scale, torch.float32, "inv_scale"),
+        cap, int(blk_begin), int(nblk),
+        _dptr(desc, torch.uint8, "desc"), _dptr(params, torch.uint8, "params"), int(nparams),
+        _dptr(w_fp8_t, torch.uint8, "w_fp8_t"), 0 if w_fp8_t is None else w_fp8_t.numel(),
+        _dptr(inv_scale_t, torch.float32, "inv_scale_t"),
+        0 if inv_scale_t is None else inv_scale_t.numel(),
+        ctypes.byref(hp), _dptr(dev_status, torch.int32, "dev_status"), _stream_handle(stream))
+    _check("fp8z_adamw_requant_step", rc)
+
+
+def fp8z_dequant(w_fp8, inv_scale, nblk, out, stream=None):
+    import torch
+    if w_fp8.numel() < nblk * BLOCK_ELEMS or out.numel() < nblk * BLOCK_ELEMS or inv_scale.numel() < nblk:
+        raise ValueError("buffers smaller than nblk blocks")
+    rc = lib().fp8z_dequant(_dptr(w_fp8, torch.uint8, "w_fp8"),
+                            _dptr(inv_scale, torch.float32, "inv_scale"), int(nblk),
+                            _dptr(out, torch.float32, "out"), _stream_handle(stream))
+    _check("fp8z_dequant", rc)
+
+
+def fp8z_transpose_fp8(w_fp8, inv_scale, entry, out, inv_scale_t, stream=None):
+    """entry: one param_entry_dtype record (host).  out: uint8 [E, W, H];
+    inv_scale_t: float32 [E, Wb, Hb]."""
+    import torch
+    ent = np.array([entry], dtype=param_entry_dtype)
+    E, H, W = int(entry["e"]), int(entry["rows"]), int(entry["cols"])
+    nb = E * int(entry["hb"]) * int(entry["wb"])
+    if out.numel() < E * H * W or inv_scale_t.numel() < nb:
+        raise ValueError("output buffers too small")
+    if w_fp8.numel() < (int(entry["blk_offset"]) + nb) * BLOCK_ELEMS:
+        raise ValueError("w_fp8 does not hold the param's blocks")
+    rc = lib().fp8z_transpose_fp8(_dptr(w_fp8, torch.uint8, "w_fp8"),
+                                  _dptr(inv_scale, torch.float32, "inv_scale"), ent.ctypes.data,
+                                  _dptr(out, torch.uint8, "out"),
+                                  _dptr(inv_scale_t, torch.float32, "inv_scale_t"),
+                                  _stream_handle(stream))
+    _check("fp8z_transpose_fp8", rc)
+
+
+def fp8z_e4m3_encode_bits(first_bits, n, out, stream=None):
+    import torch
+    if out.numel() < n:
+        raise ValueError("out too small")
+    rc = lib().fp8z_e4m3_encode_bits(int(first_bits) & 0xFFFFFFFF, int(n),
+                                     _dptr(out, torch.uint8, "out"), _stream_handle(stream))
+    _check("fp8z_e4m3_encode_bits", rc)
+
+
+def fp8z_watchdog_selftest(dev_status, timeout_ns, stream=None):
+    import torch
+    rc = lib().fp8z_watchdog_selftest(_dptr(dev_status, torch.int32, "dev_status"),
+                                      int(timeout_ns), _stream_handle(stream))
+    _check("fp8z_watchdog_selftest", rc)

@@ -27,10 +27,12 @@
  *     descriptor, a wait that ran out of time) are written with an atomic
  *     compare-and-swap into *dev_status (device int32, must start at 0) when
  *     the caller passes one; read it after synchronizing the stream.
- *   - Device pointers must be 16-byte aligned.  A block is 128x128 = 16384
- *     elements; float buffers hold [nblocks,128,128] fp32 row-major per block,
- *     byte buffers [nblocks,128,128] E4M3 codes, scale buffers one fp32 per
- *     block.
+ *   - Alignment: float and byte block buffers (p, g, m, v, w_fp8, w_fp8_t,
+ *     dequant output) 16 bytes; scale buffers, descriptors and dev_status 4
+ *     bytes; the param table 8 bytes.  A misaligned pointer gives FP8Z_EALIGN.
+ *   - A block is 128x128 = 16384 elements; float buffers hold
+ *     [nblocks,128,128] fp32, row-major inside each block; byte buffers the
+ *     same layout of E4M3 codes; scale buffers one fp32 per block.
  *   - Return codes are fp8z_status values; fp8z_status_string() names them.
  */
 #ifndef FP8Z_H
@@ -42,17 +44,23 @@
 extern "C" {
 #endif
 
+#if defined(__GNUC__)
+#define FP8Z_API __attribute__((visibility("default")))
+#else
+#define FP8Z_API
+#endif
+
 #define FP8Z_BLOCK 128
 #define FP8Z_BLOCK_ELEMS 16384
 
 typedef enum {
     FP8Z_OK = 0,
     FP8Z_EINVAL = -1,        /* bad argument (null, negative, out of range)  */
-    FP8Z_EALIGN = -2,        /* pointer not 16-byte aligned                  */
+    FP8Z_EALIGN = -2,        /* pointer not aligned as required              */
     FP8Z_ENOSPACE = -3,      /* a range does not fit the stated capacity     */
     FP8Z_ECUDA = -4,         /* a CUDA runtime call or launch failed         */
     FP8Z_ETIMEOUT = -5,      /* device: a bounded wait ran out of time       */
-    FP8Z_EUNSUPPORTED = -6   /* no sm_100-family device current              */
+    FP8Z_EUNSUPPORTED = -6   /* current device is not sm_103 (GB300)         */
 } fp8z_status;
 
 typedef enum { FP8Z_SPLIT_BLOCKWISE = 0, FP8Z_SPLIT_PARAMWISE = 1 } fp8z_split;
@@ -129,7 +137,7 @@ typedef struct {
  * Returns FP8Z_OK, FP8Z_EINVAL (bad shape/dp/split/null), FP8Z_ENOSPACE
  * (blocks_cap < capacity_blocks).  Deterministic; no device work.
  */
-int fp8z_plan_shards(const fp8z_param_shape *shapes, int32_t nparams, int32_t dp,
+FP8Z_API int fp8z_plan_shards(const fp8z_param_shape *shapes, int32_t nparams, int32_t dp,
                      int32_t split, fp8z_param_entry *params_out, fp8z_shard *shards_out,
                      fp8z_block_desc *blocks_out, int64_t blocks_cap,
                      fp8z_plan_summary *summary_out);
@@ -168,7 +176,7 @@ int fp8z_plan_shards(const fp8z_param_shape *shapes, int32_t nparams, int32_t dp
  * Returns FP8Z_OK, FP8Z_EINVAL, FP8Z_EALIGN, FP8Z_ENOSPACE (blk_begin+nblk >
  * capacity_blocks), FP8Z_EUNSUPPORTED, FP8Z_ECUDA.  nblk == 0 launches nothing.
  */
-int fp8z_adamw_requant_step(float *p, const float *g, float *m, float *v,
+FP8Z_API int fp8z_adamw_requant_step(float *p, const float *g, float *m, float *v,
                             uint8_t *w_fp8, float *inv_scale, int64_t capacity_blocks,
                             int64_t blk_begin, int64_t nblk,
                             const fp8z_block_desc *desc,
@@ -184,7 +192,7 @@ int fp8z_adamw_requant_step(float *p, const float *g, float *m, float *v,
  * w_fp8: device u8 [nblk,128,128]; inv_scale: device f32 [nblk];
  * out: device f32 [nblk,128,128].  Returns FP8Z_OK / EINVAL / EALIGN / ECUDA.
  */
-int fp8z_dequant(const uint8_t *w_fp8, const float *inv_scale, int64_t nblk,
+FP8Z_API int fp8z_dequant(const uint8_t *w_fp8, const float *inv_scale, int64_t nblk,
                  float *out, void *stream);
 
 /*
@@ -200,7 +208,7 @@ int fp8z_dequant(const uint8_t *w_fp8, const float *inv_scale, int64_t nblk,
  *   16 (an unaligned row length takes a byte-store path).
  * Returns FP8Z_OK / EINVAL / EALIGN / ECUDA.
  */
-int fp8z_transpose_fp8(const uint8_t *w_fp8, const float *inv_scale,
+FP8Z_API int fp8z_transpose_fp8(const uint8_t *w_fp8, const float *inv_scale,
                        const fp8z_param_entry *entry, uint8_t *out, float *inv_scale_t,
                        void *stream);
 
@@ -211,7 +219,7 @@ int fp8z_transpose_fp8(const uint8_t *w_fp8, const float *inv_scale,
  * Exposes the step's float->E4M3 cast on its own so it can be checked over
  * all 2^32 inputs ("FP8-Flow-MoE" §3.1 value formula).
  */
-int fp8z_e4m3_encode_bits(uint32_t first_bits, int64_t n, uint8_t *out, void *stream);
+FP8Z_API int fp8z_e4m3_encode_bits(uint32_t first_bits, int64_t n, uint8_t *out, void *stream);
 
 /*
  * fp8z_watchdog_selftest -- launches one CTA that waits on a barrier nothing
@@ -220,10 +228,10 @@ int fp8z_e4m3_encode_bits(uint32_t first_bits, int64_t n, uint8_t *out, void *st
  * int32, starting at 0) and returns.  Lets a test see the device error path
  * without any fault or hang.  timeout_ns in [0, 10^10].
  */
-int fp8z_watchdog_selftest(int32_t *dev_status, int64_t timeout_ns, void *stream);
+FP8Z_API int fp8z_watchdog_selftest(int32_t *dev_status, int64_t timeout_ns, void *stream);
 
 /* Static string naming a status code (never NULL). */
-const char *fp8z_status_string(int status);
+FP8Z_API const char *fp8z_status_string(int status);
 
 #ifdef __cplusplus
 }
