@@ -147,6 +147,18 @@ class ClockSampler:
                 "reasons": sorted(reasons)}
 
 
+def max_over_ranks(x: float, device=None) -> float:
+    """The largest value of x over all ranks (the job's time is the slowest
+    rank's); x itself when not running distributed."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def host_mem_gb():
     try:
         for line in open("/proc/meminfo"):
@@ -208,6 +220,8 @@ def run_ours(args):
     fp8z.lib()
 
     w = workloads.get(args.workload)
+    if args.max_elems:
+        w = workloads.scaled(w, args.max_elems)
     free, total = torch.cuda.mem_get_info(dev)
     per_elem = 16 + 1 + (1 if w.transposed else 0)
     budget = int((free - (6 << 30)) / per_elem)
@@ -281,12 +295,7 @@ def run_ours(args):
     if status.item() != 0:
         raise RuntimeError(fp8z.fp8z_status_string(status.item()))
     per_step_ms = [ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)]
-    total_ms = ev[0].elapsed_time(ev[-1])
-    if ws > 1:
-        import torch.distributed as dist
-        tt = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        total_ms = float(tt.item())
+    total_ms = max_over_ranks(ev[0].elapsed_time(ev[-1]), dev)
     value = real * args.steps * ws / (total_ms / 1e3) / 1e9
 
     # algorithmic bytes per launch: read g, p, m, v; write p, m, v, codes
@@ -300,7 +309,8 @@ def run_ours(args):
     traffic = profiled_traffic() if (scaled_note is None and launches_per_step == 1) else None
 
     # ---- end to end through the C ABI with pinned host buffers
-    e2e = run_e2e(args, w, state, q, inv, wt, it, desc, pdev, params, shards, hp_kw, t, dev, ws)
+    e2e = None if args.no_e2e else run_e2e(args, w, state, q, inv, wt, it, desc, pdev, params,
+                                            shards, hp_kw, t, dev, ws)
 
     line = {
         "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": ws,
@@ -309,7 +319,7 @@ def run_ours(args):
         "data": "synthetic",
         "config": {"workload": w.name, "params": len(w.shapes), "elements": real, "blocks": nblk_run,
                    "dp_shards": w.dp, "column_major_copy": w.transposed, "step": step0,
-                   "l2": "state 96 GB >> 129 MB L2: no flush between steps",
+                   "l2": f"state {cap * BLK * 16 / 1e9:.0f} GB >> 129 MB L2: no flush between steps",
                    "launches_per_step": launches_per_step, "scaled": scaled_note,
                    "hbm_gbs": round(achieved, 1),
                    "frac_of_nominal_8tbs": round(achieved / NOMINAL_HBM_GBS, 4)},
@@ -408,12 +418,7 @@ def run_e2e(args, w, state, q, inv, wt, it, desc, pdev, params, shards, hp_kw, t
     for i in range(steps):
         one(t + 1 + i)
     torch.cuda.synchronize(dev)
-    secs = time.perf_counter() - t0
-    if ws > 1:
-        import torch.distributed as dist
-        tt = torch.tensor([secs], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        secs = float(tt.item())
+    secs = max_over_ranks(time.perf_counter() - t0, dev)
     real = sum(u[3] for u in units)
     return {"value": round(real * steps * ws / secs / 1e9, 4), "unit": UNIT,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
@@ -470,8 +475,11 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="flat6e9")
-    ap.add_argument("--cpu-blocks", type=int, default=12288)
+    ap.add_argument("--cpu-blocks", type=int, default=24576)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--max-elems", type=int, default=0,
+                    help="run a smaller workload of the same kind (profiling cases)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         ap.error("--warmup must be >= 3")

@@ -101,6 +101,15 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
         : "memory");
 }
 
+// The same copy without an L2 cache hint.
+__device__ __forceinline__ void bulk_g2s_nohint(uint32_t dst, const void* src, uint32_t bytes,
+                                                uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+        "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
 // ------------------------------------------------------------- E4M3 cast
 // Two floats -> two E4M3 codes, round to nearest even, saturating to ±448
 // (NaN stays NaN).  `lo` lands in the low byte.

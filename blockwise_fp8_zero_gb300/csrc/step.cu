@@ -34,17 +34,51 @@
 namespace fp8z {
 namespace {
 
+// Build-time shape of the pipeline.  The defaults won a sweep on GB300 at
+// 6e9 elements (28.0 ms per step): a deeper ring is faster (4 and 5 stages
+// lose 2-6 %), plain bulk loads beat the L2 evict-first hint (+1.5 %),
+// streaming stores of the FP32 outputs help once the loads are plain, loading
+// the next block's descriptor early helps a little (+0.2 %).  Losers dropped
+// from the code: L2 prefetch ahead of the ring (-35 %), one contiguous block
+// range per CTA (-2.5 %), streaming stores of the E4M3 bytes (-2.5 %), two
+// rows per warp per stage with 3 stages (-10 %).
+//   FP8Z_RING             shared-memory stages in the ring
+//   FP8Z_ROWS_PER_WARP    block rows each consumer warp takes per stage
+//   FP8Z_STORE_STREAMING  1: p', m', v' stored with the streaming (.cs) hint
+//   FP8Z_LOAD_EVICT_FIRST 1: bulk loads carry an L2 evict-first policy
+//   FP8Z_PREFETCH_NEXT    1: a block's descriptor and copy target are loaded
+//                         one block ahead of their use
+#ifndef FP8Z_RING
+#define FP8Z_RING 6
+#endif
+#ifndef FP8Z_ROWS_PER_WARP
+#define FP8Z_ROWS_PER_WARP 1
+#endif
+#ifndef FP8Z_STORE_STREAMING
+#define FP8Z_STORE_STREAMING 1
+#endif
+#ifndef FP8Z_LOAD_EVICT_FIRST
+#define FP8Z_LOAD_EVICT_FIRST 0
+#endif
+#ifndef FP8Z_PREFETCH_NEXT
+#define FP8Z_PREFETCH_NEXT 1
+#endif
+
 constexpr int kBlk = FP8Z_BLOCK;
 constexpr int kBlkElems = FP8Z_BLOCK_ELEMS;
 constexpr int kConsumerWarps = 16;
 constexpr int kConsumers = kConsumerWarps * 32;
 constexpr int kThreads = kConsumers + 32;               // + one producer warp
-constexpr int kStageRows = kConsumerWarps;              // one row per consumer warp
-constexpr int kStageElems = kStageRows * kBlk;          // 2048
-constexpr int kStagesPerBlock = kBlk / kStageRows;      // 8
-constexpr uint32_t kTensorStageBytes = kStageElems * 4; // 8 KB
-constexpr uint32_t kStageBytes = 4 * kTensorStageBytes; // g, p, m, v: 32 KB
-constexpr int kRing = 6;                                // 192 KB of stages
+constexpr int kRowsPerWarp = FP8Z_ROWS_PER_WARP;
+constexpr int kStageRows = kConsumerWarps * kRowsPerWarp;
+constexpr int kStageElems = kStageRows * kBlk;
+constexpr int kStagesPerBlock = kBlk / kStageRows;
+constexpr int kKeep = kBlkElems / (kConsumers * 4);     // float4 of p' kept per thread: 8
+constexpr uint32_t kTensorStageBytes = kStageElems * 4;
+constexpr uint32_t kStageBytes = 4 * kTensorStageBytes; // g, p, m, v
+constexpr int kRing = FP8Z_RING;
+static_assert(kBlk % kStageRows == 0, "stage rows must divide the block");
+static_assert(kKeep * kConsumers * 4 == kBlkElems, "consumer layout");
 
 constexpr size_t kRingBytes = size_t(kRing) * kStageBytes;
 constexpr size_t kTileBytes = kBlkElems;                 // 16 KB byte tile
@@ -144,6 +178,11 @@ struct BlockInfo {
     int param, e, brow, bcol;
 };
 
+// Where a block's column-major copy goes (loaded one block ahead).
+struct ParamInfo {
+    int64_t e, H, W, hb, wb, t_off, ts_off;
+};
+
 __device__ __forceinline__ BlockInfo load_desc(const StepArgs& A, int64_t blk) {
     BlockInfo bi{kBlk, kBlk, -1, 0, 0, 0};
     if (A.desc) {
@@ -157,6 +196,103 @@ __device__ __forceinline__ BlockInfo load_desc(const StepArgs& A, int64_t blk) {
         bi.vc = int(valid >> 16);
     }
     return bi;
+}
+
+__device__ __forceinline__ ParamInfo load_param(const StepArgs& A, const BlockInfo& bi) {
+    ParamInfo pi{0, 0, 0, 0, 0, 0, 0};
+    if (A.w_fp8_t != nullptr && bi.param >= 0 && bi.param < A.nparams) {
+        const fp8z_param_entry* pe = A.params + bi.param;
+        pi.e = __ldg(&pe->e);
+        pi.H = __ldg(&pe->rows);
+        pi.W = __ldg(&pe->cols);
+        pi.hb = __ldg(&pe->hb);
+        pi.wb = __ldg(&pe->wb);
+        pi.t_off = __ldg(&pe->t_offset);
+        pi.ts_off = __ldg(&pe->t_scale_offset);
+    }
+    return pi;
+}
+
+__device__ __forceinline__ void store4(float* dst, float4 x) {
+#if FP8Z_STORE_STREAMING
+    __stcs(reinterpret_cast<float4*>(dst), x);
+#else
+    *reinterpret_cast<float4*>(dst) = x;
+#endif
+}
+
+__device__ __forceinline__ void store_word(uint8_t* dst, uint32_t x) {
+    *reinterpret_cast<uint32_t*>(dst) = x;
+}
+
+// Which blocks a CTA owns: blocks are dealt round-robin, so at any moment the
+// CTAs stream neighbouring 64 KB blocks (DRAM page locality).  The grid never
+// exceeds nblk, so every CTA owns at least one block.
+struct BlockSched {
+    int64_t first, stride, count;
+    __device__ __forceinline__ int64_t blk(int64_t i) const { return first + i * stride; }
+};
+
+__device__ __forceinline__ BlockSched block_sched(int64_t blk_begin, int64_t nblk) {
+    return BlockSched{blk_begin + blockIdx.x, gridDim.x,
+                      (nblk - blockIdx.x + gridDim.x - 1) / gridDim.x};
+}
+
+// Column-major copy of one block: the quantized words go through a swizzled
+// shared tile; each warp then writes four output rows per pass, 128
+// contiguous bytes per warp store.  Returns false when a wait gave up.
+__device__ __forceinline__ bool column_major_copy(const StepArgs& A, const BlockInfo& bi,
+                                                  const ParamInfo& pi, const uint32_t (&words)[kKeep],
+                                                  float inv, uint32_t* tile, uint32_t tile_bar,
+                                                  uint32_t& tile_phase, const Watchdog& wd,
+                                                  int tid, int warp, int lane) {
+    const int64_t H = pi.H, W = pi.W;
+    const bool ok = bi.param < A.nparams && bi.e >= 0 && bi.e < pi.e && bi.brow >= 0 &&
+                    bi.brow < pi.hb && bi.bcol >= 0 && bi.bcol < pi.wb &&
+                    bi.vr == imin64(kBlk, H - bi.brow * int64_t(kBlk)) &&
+                    bi.vc == imin64(kBlk, W - bi.bcol * int64_t(kBlk)) && pi.t_off >= 0 &&
+                    pi.ts_off >= 0 && pi.t_off + (bi.e + 1) * H * W <= A.w_fp8_t_bytes &&
+                    pi.ts_off + (bi.e + 1) * pi.hb * pi.wb <= A.inv_scale_t_count;
+    if (!ok) {
+        if (tid == 0) report_status(A.dev_status, FP8Z_EINVAL);
+        return true;
+    }
+    const int64_t t_base = pi.t_off + bi.e * H * W;
+#pragma unroll
+    for (int k = 0; k < kKeep; ++k) {
+        const int row = k * kConsumerWarps + warp;
+        tile[row * 32 + (lane ^ tile_swz(row))] = words[k];
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(tile_bar);
+    if (!mbar_wait_bounded(tile_bar, tile_phase, wd)) return false;
+    tile_phase ^= 1;
+
+    if (tid == 0) A.inv_scale_t[pi.ts_off + bi.e * pi.wb * pi.hb + bi.bcol * pi.hb + bi.brow] = inv;
+    const bool aligned = ((t_base | H) & 3) == 0;
+    const int r0 = lane * 4;                           // input rows r0..r0+3
+    uint8_t* out_blk = A.w_fp8_t + t_base + bi.brow * int64_t(kBlk);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int cg = warp + h * kConsumerWarps;      // input cols 4cg..4cg+3
+        uint32_t w4[4];
+#pragma unroll
+        for (int ii = 0; ii < 4; ++ii) w4[ii] = tile[(r0 + ii) * 32 + (cg ^ tile_swz(r0 + ii))];
+        uint32_t o[4];
+        transpose4x4(w4[0], w4[1], w4[2], w4[3], o[0], o[1], o[2], o[3]);
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+            const int c = 4 * cg + cc;
+            if (c >= bi.vc || r0 >= bi.vr) continue;
+            uint8_t* dst = out_blk + (bi.bcol * int64_t(kBlk) + c) * H + r0;
+            if (aligned && r0 + 3 < bi.vr) {
+                store_word(dst, o[cc]);
+            } else {
+                for (int b = 0; b < 4 && r0 + b < bi.vr; ++b) dst[b] = uint8_t(o[cc] >> (8 * b));
+            }
+        }
+    }
+    return true;
 }
 
 __global__ void __launch_bounds__(kThreads, 1) fp8z_step_kernel(const StepArgs A) {
@@ -189,30 +325,38 @@ __global__ void __launch_bounds__(kThreads, 1) fp8z_step_kernel(const StepArgs A
     __syncthreads();
 
     const Watchdog wd{abort_flag, A.dev_status, A.timeout_ns};
-    // grid <= nblk, so every CTA owns at least one block
-    const int64_t nmine = (A.nblk - blockIdx.x + gridDim.x - 1) / gridDim.x;
+    const BlockSched sched = block_sched(A.blk_begin, A.nblk);
+    const int64_t nmine = sched.count;
 
     if (warp == kConsumerWarps) {
         // ------------------------------------------------------ producer
         if (lane != 0) return;
+#if FP8Z_LOAD_EVICT_FIRST
         const uint64_t pol = l2_evict_first_policy();
+#endif
         const uint32_t ring0 = smem_addr(ring);
         int slot = 0;
         uint32_t phase = 0;
         int64_t issued = 0;
         for (int64_t i = 0; i < nmine; ++i) {
-            const int64_t blk = A.blk_begin + blockIdx.x + i * gridDim.x;
-            const size_t base = size_t(blk) * kBlkElems;
+            const size_t base = size_t(sched.blk(i)) * kBlkElems;
             for (int k = 0; k < kStagesPerBlock; ++k) {
                 if (!mbar_wait_bounded(empty0 + 8 * slot, phase ^ 1, wd)) goto drain;
                 const uint32_t full = full0 + 8 * slot;
                 mbar_arrive_expect_tx(full, kStageBytes);
                 const uint32_t dst = ring0 + slot * kStageBytes;
                 const size_t off = base + size_t(k) * kStageElems;
+#if FP8Z_LOAD_EVICT_FIRST
                 bulk_g2s(dst + 0 * kTensorStageBytes, A.g + off, kTensorStageBytes, full, pol);
                 bulk_g2s(dst + 1 * kTensorStageBytes, A.p + off, kTensorStageBytes, full, pol);
                 bulk_g2s(dst + 2 * kTensorStageBytes, A.m + off, kTensorStageBytes, full, pol);
                 bulk_g2s(dst + 3 * kTensorStageBytes, A.v + off, kTensorStageBytes, full, pol);
+#else
+                bulk_g2s_nohint(dst + 0 * kTensorStageBytes, A.g + off, kTensorStageBytes, full);
+                bulk_g2s_nohint(dst + 1 * kTensorStageBytes, A.p + off, kTensorStageBytes, full);
+                bulk_g2s_nohint(dst + 2 * kTensorStageBytes, A.m + off, kTensorStageBytes, full);
+                bulk_g2s_nohint(dst + 3 * kTensorStageBytes, A.v + off, kTensorStageBytes, full);
+#endif
                 ++issued;
                 if (++slot == kRing) { slot = 0; phase ^= 1; }
             }
@@ -229,51 +373,73 @@ __global__ void __launch_bounds__(kThreads, 1) fp8z_step_kernel(const StepArgs A
     }
 
     // ---------------------------------------------------------- consumers
+    // Stage k holds block rows [k*kStageRows, (k+1)*kStageRows); within it,
+    // warp w takes rows r*kConsumerWarps + w (r < kRowsPerWarp), each lane four
+    // consecutive columns, so every warp access is 512 contiguous bytes.
     const int col = lane * 4;
     const bool transposed = (A.w_fp8_t != nullptr);
     int slot = 0;
     uint32_t phase = 0;
     uint32_t tile_phase = 0;
+#if FP8Z_PREFETCH_NEXT
+    BlockInfo bi = load_desc(A, sched.blk(0));
+#endif
 
     for (int64_t i = 0; i < nmine; ++i) {
-        const int64_t blk = A.blk_begin + blockIdx.x + i * gridDim.x;
+        const int64_t blk = sched.blk(i);
         const size_t base = size_t(blk) * kBlkElems;
+#if FP8Z_PREFETCH_NEXT
+        // descriptor of the next block and this block's copy target, issued a
+        // block ahead of their use so their latency is hidden
+        const BlockInfo bnext = (i + 1 < nmine) ? load_desc(A, sched.blk(i + 1)) : bi;
+        const ParamInfo pi = load_param(A, bi);
+#else
         const BlockInfo bi = load_desc(A, blk);
+#endif
 
-        float4 keep[kStagesPerBlock];
+        float4 keep[kKeep];
         float lmax = 0.0f;
 #pragma unroll
         for (int k = 0; k < kStagesPerBlock; ++k) {
             if (!mbar_wait_bounded(full0 + 8 * slot, phase, wd)) return;
             const float* st = ring + size_t(slot) * (kStageBytes / 4);
-            const float4 g4 = lds4(st + 0 * kStageElems + tid * 4);
-            const float4 p4 = lds4(st + 1 * kStageElems + tid * 4);
-            const float4 m4 = lds4(st + 2 * kStageElems + tid * 4);
-            const float4 v4 = lds4(st + 3 * kStageElems + tid * 4);
+            float4 g4[kRowsPerWarp], p4[kRowsPerWarp], m4[kRowsPerWarp], v4[kRowsPerWarp];
+#pragma unroll
+            for (int r = 0; r < kRowsPerWarp; ++r) {
+                const int e0 = r * kConsumers * 4 + tid * 4;
+                g4[r] = lds4(st + 0 * kStageElems + e0);
+                p4[r] = lds4(st + 1 * kStageElems + e0);
+                m4[r] = lds4(st + 2 * kStageElems + e0);
+                v4[r] = lds4(st + 3 * kStageElems + e0);
+            }
             __syncwarp();
             if (lane == 0) mbar_arrive(empty0 + 8 * slot);
             if (++slot == kRing) { slot = 0; phase ^= 1; }
 
-            float4 p1, m1, v1;
-            adamw1(A, p4.x, g4.x, m4.x, v4.x, p1.x, m1.x, v1.x);
-            adamw1(A, p4.y, g4.y, m4.y, v4.y, p1.y, m1.y, v1.y);
-            adamw1(A, p4.z, g4.z, m4.z, v4.z, p1.z, m1.z, v1.z);
-            adamw1(A, p4.w, g4.w, m4.w, v4.w, p1.w, m1.w, v1.w);
+#pragma unroll
+            for (int r = 0; r < kRowsPerWarp; ++r) {
+                float4 p1, m1, v1;
+                adamw1(A, p4[r].x, g4[r].x, m4[r].x, v4[r].x, p1.x, m1.x, v1.x);
+                adamw1(A, p4[r].y, g4[r].y, m4[r].y, v4[r].y, p1.y, m1.y, v1.y);
+                adamw1(A, p4[r].z, g4[r].z, m4[r].z, v4[r].z, p1.z, m1.z, v1.z);
+                adamw1(A, p4[r].w, g4[r].w, m4[r].w, v4[r].w, p1.w, m1.w, v1.w);
 
-            const int row = k * kStageRows + warp;
-            if (row >= bi.vr || col + 3 >= bi.vc) {     // padding of a ragged edge block
-                const bool rv = row < bi.vr;
-                if (!(rv && col + 0 < bi.vc)) { p1.x = 0.f; m1.x = 0.f; v1.x = 0.f; }
-                if (!(rv && col + 1 < bi.vc)) { p1.y = 0.f; m1.y = 0.f; v1.y = 0.f; }
-                if (!(rv && col + 2 < bi.vc)) { p1.z = 0.f; m1.z = 0.f; v1.z = 0.f; }
-                if (!(rv && col + 3 < bi.vc)) { p1.w = 0.f; m1.w = 0.f; v1.w = 0.f; }
+                const int kk = k * kRowsPerWarp + r;
+                const int row = kk * kConsumerWarps + warp;
+                if (row >= bi.vr || col + 3 >= bi.vc) {     // padding of a ragged edge block
+                    const bool rv = row < bi.vr;
+                    if (!(rv && col + 0 < bi.vc)) { p1.x = 0.f; m1.x = 0.f; v1.x = 0.f; }
+                    if (!(rv && col + 1 < bi.vc)) { p1.y = 0.f; m1.y = 0.f; v1.y = 0.f; }
+                    if (!(rv && col + 2 < bi.vc)) { p1.z = 0.f; m1.z = 0.f; v1.z = 0.f; }
+                    if (!(rv && col + 3 < bi.vc)) { p1.w = 0.f; m1.w = 0.f; v1.w = 0.f; }
+                }
+                const size_t off = base + size_t(row) * kBlk + col;
+                store4(A.p + off, p1);
+                store4(A.m + off, m1);
+                store4(A.v + off, v1);
+                keep[kk] = p1;
+                lmax = absmax4(lmax, p1);
             }
-            const size_t off = base + size_t(row) * kBlk + col;
-            *reinterpret_cast<float4*>(A.p + off) = p1;
-            *reinterpret_cast<float4*>(A.m + off) = m1;
-            *reinterpret_cast<float4*>(A.v + off) = v1;
-            keep[k] = p1;
-            lmax = absmax4(lmax, p1);
         }
 
         // ---- block amax: warp shuffle, then one exchange through shared memory
@@ -294,73 +460,28 @@ __global__ void __launch_bounds__(kThreads, 1) fp8z_step_kernel(const StepArgs A
         if (tid == 0) A.inv_scale[blk] = inv;
 
         // ---- quantize the kept p' and store the row-major E4M3 block
-        uint32_t words[kStagesPerBlock];
+        uint32_t words[kKeep];
 #pragma unroll
-        for (int k = 0; k < kStagesPerBlock; ++k) {
+        for (int k = 0; k < kKeep; ++k) {
             const float4 x = keep[k];
             words[k] = pack_e4m3x4(__fmul_rn(x.x, s), __fmul_rn(x.y, s), __fmul_rn(x.z, s),
                                    __fmul_rn(x.w, s));
-            const int row = k * kStageRows + warp;
-            *reinterpret_cast<uint32_t*>(A.w_fp8 + base + size_t(row) * kBlk + col) = words[k];
+            const int row = k * kConsumerWarps + warp;
+            store_word(A.w_fp8 + base + size_t(row) * kBlk + col, words[k]);
         }
 
         // ---- optional column-major copy of the param + transposed scale grid
-        if (!transposed || bi.param < 0) continue;
-        bool ok = bi.param < A.nparams;
-        int64_t H = 0, W = 0, t_base = 0, s_idx = 0;
-        if (ok) {
-            const fp8z_param_entry* pe = A.params + bi.param;
-            const int64_t pe_e = __ldg(&pe->e);
-            H = __ldg(&pe->rows);
-            W = __ldg(&pe->cols);
-            const int64_t hb = __ldg(&pe->hb), wb = __ldg(&pe->wb);
-            const int64_t t_off = __ldg(&pe->t_offset), ts_off = __ldg(&pe->t_scale_offset);
-            ok = bi.e >= 0 && bi.e < pe_e && bi.brow >= 0 && bi.brow < hb && bi.bcol >= 0 &&
-                 bi.bcol < wb && bi.vr == imin64(kBlk, H - bi.brow * int64_t(kBlk)) &&
-                 bi.vc == imin64(kBlk, W - bi.bcol * int64_t(kBlk)) && t_off >= 0 &&
-                 ts_off >= 0 && t_off + (bi.e + 1) * H * W <= A.w_fp8_t_bytes &&
-                 ts_off + (bi.e + 1) * hb * wb <= A.inv_scale_t_count;
-            t_base = t_off + bi.e * H * W;
-            s_idx = ts_off + bi.e * wb * hb + bi.bcol * hb + bi.brow;
+        if (transposed && bi.param >= 0) {
+#if !FP8Z_PREFETCH_NEXT
+            const ParamInfo pi = load_param(A, bi);
+#endif
+            if (!column_major_copy(A, bi, pi, words, inv, tile, tile_bar, tile_phase, wd, tid, warp,
+                                   lane))
+                return;
         }
-        if (!ok) {
-            if (tid == 0) report_status(A.dev_status, FP8Z_EINVAL);
-            continue;
-        }
-#pragma unroll
-        for (int k = 0; k < kStagesPerBlock; ++k) {
-            const int row = k * kStageRows + warp;
-            tile[row * 32 + (lane ^ tile_swz(row))] = words[k];
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(tile_bar);
-        if (!mbar_wait_bounded(tile_bar, tile_phase, wd)) return;
-        tile_phase ^= 1;
-
-        if (tid == 0) A.inv_scale_t[s_idx] = inv;
-        const bool aligned = ((t_base | H) & 3) == 0;
-        const int r0 = lane * 4;                       // input rows r0..r0+3
-        uint8_t* out_blk = A.w_fp8_t + t_base + bi.brow * int64_t(kBlk);
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int cg = warp + h * kConsumerWarps;  // input cols 4cg..4cg+3
-            uint32_t w4[4];
-#pragma unroll
-            for (int ii = 0; ii < 4; ++ii) w4[ii] = tile[(r0 + ii) * 32 + (cg ^ tile_swz(r0 + ii))];
-            uint32_t o[4];
-            transpose4x4(w4[0], w4[1], w4[2], w4[3], o[0], o[1], o[2], o[3]);
-#pragma unroll
-            for (int cc = 0; cc < 4; ++cc) {
-                const int c = 4 * cg + cc;
-                if (c >= bi.vc || r0 >= bi.vr) continue;
-                uint8_t* dst = out_blk + (bi.bcol * int64_t(kBlk) + c) * H + r0;
-                if (aligned && r0 + 3 < bi.vr) {
-                    *reinterpret_cast<uint32_t*>(dst) = o[cc];
-                } else {
-                    for (int b = 0; b < 4 && r0 + b < bi.vr; ++b) dst[b] = uint8_t(o[cc] >> (8 * b));
-                }
-            }
-        }
+#if FP8Z_PREFETCH_NEXT
+        bi = bnext;
+#endif
     }
 }
 
