@@ -308,6 +308,8 @@ def run_ours(args):
     peak, peak_src = measured_peak()
     traffic = profiled_traffic() if (scaled_note is None and launches_per_step == 1) else None
 
+    aux = None if args.no_aux else time_aux_kernels(w, q, inv, params, dev, stream, peak, g=state["g"])
+
     # ---- end to end through the C ABI with pinned host buffers
     e2e = None if args.no_e2e else run_e2e(args, w, state, q, inv, wt, it, desc, pdev, params,
                                             shards, hp_kw, t, dev, ws)
@@ -328,6 +330,7 @@ def run_ours(args):
                      "algorithmic_bytes": alg_bytes_step // launches_per_step,
                      "peak_source": peak_src,
                      "kernel": "fp8z_step_kernel", "kernel_ms": round(avg_launch_s * 1e3, 4)},
+        "aux_kernels": aux,
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
         "e2e": e2e,
@@ -339,6 +342,79 @@ def run_ours(args):
     if ws > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def time_aux_kernels(w, q, inv, params, dev, stream, peak, reps=5, g=None):
+    """Dequantize, the standalone column-major transpose, unfold/fold of the
+    FP32 grad and unfold of the E4M3 codes, each timed with CUDA events against
+    its algorithmic bytes (dequant: 1 B read + 4 B written per element + 4 B per
+    block; transpose: 1 + 1 B per element + 8 B per block; FP32 fold/unfold:
+    4 + 4 B per element; byte unfold: 1 + 1 B per element)."""
+    import torch
+    from blockwise_fp8_zero_gb300 import fp8z
+    out = {}
+    nblk = inv.numel()
+    try:
+        buf = torch.empty(nblk * BLK, dtype=torch.float32, device=dev)
+    except RuntimeError:
+        return None
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    with torch.cuda.stream(stream):
+        fp8z.fp8z_dequant(q, inv, nblk, buf, stream=stream)
+        ev[0].record(stream)
+        for _ in range(reps):
+            fp8z.fp8z_dequant(q, inv, nblk, buf, stream=stream)
+        ev[1].record(stream)
+    torch.cuda.synchronize(dev)
+    ms = ev[0].elapsed_time(ev[1]) / reps
+    nbytes = nblk * (BLK * 5 + 4)
+    out["fp8z_dequant"] = {"ms": round(ms, 4), "bytes": nbytes, "gbs": round(nbytes / ms / 1e6, 1),
+                           "frac": round(nbytes / ms / 1e6 / peak, 4)}
+    del buf
+    pe = params[0]
+    E, H, W = int(pe["e"]), int(pe["rows"]), int(pe["cols"])
+    nb = E * int(pe["hb"]) * int(pe["wb"])
+    t_out = torch.empty(E * W * H, dtype=torch.uint8, device=dev)
+    t_inv = torch.empty(nb, dtype=torch.float32, device=dev)
+    with torch.cuda.stream(stream):
+        fp8z.fp8z_transpose_fp8(q, inv, pe, t_out, t_inv, stream=stream)
+        ev[0].record(stream)
+        for _ in range(reps):
+            fp8z.fp8z_transpose_fp8(q, inv, pe, t_out, t_inv, stream=stream)
+        ev[1].record(stream)
+    torch.cuda.synchronize(dev)
+    ms = ev[0].elapsed_time(ev[1]) / reps
+    nbytes = E * H * W * 2 + nb * 8
+    out["fp8z_transpose_fp8"] = {"ms": round(ms, 4), "bytes": nbytes, "gbs": round(nbytes / ms / 1e6, 1),
+                                 "frac": round(nbytes / ms / 1e6 / peak, 4),
+                                 "param": f"{E}x{H}x{W}"}
+    del t_out, t_inv
+
+    def timed(fn, nbytes, label):
+        with torch.cuda.stream(stream):
+            fn()
+            ev[0].record(stream)
+            for _ in range(reps):
+                fn()
+            ev[1].record(stream)
+        torch.cuda.synchronize(dev)
+        ms_ = ev[0].elapsed_time(ev[1]) / reps
+        out[label] = {"ms": round(ms_, 4), "bytes": nbytes, "gbs": round(nbytes / ms_ / 1e6, 1),
+                      "frac": round(nbytes / ms_ / 1e6 / peak, 4), "param": f"{E}x{H}x{W}"}
+
+    if g is not None and len(params) == 1:
+        try:
+            rm = torch.empty(E * H * W, dtype=torch.float32, device=dev)
+        except RuntimeError:
+            return out
+        # unfold then fold back: g ends exactly as it started
+        timed(lambda: fp8z.fp8z_unfold(g, pe, rm, stream=stream), 8 * E * H * W, "fp8z_unfold_f32")
+        timed(lambda: fp8z.fp8z_fold(rm, pe, g, stream=stream), 8 * E * H * W, "fp8z_fold_f32")
+        del rm
+        qb = torch.empty(E * H * W, dtype=torch.uint8, device=dev)
+        timed(lambda: fp8z.fp8z_unfold(q, pe, qb, stream=stream), 2 * E * H * W, "fp8z_unfold_e4m3")
+        del qb
+    return out
 
 
 def run_e2e(args, w, state, q, inv, wt, it, desc, pdev, params, shards, hp_kw, t, dev, ws):
@@ -478,6 +554,7 @@ def main():
     ap.add_argument("--cpu-blocks", type=int, default=24576)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-aux", action="store_true", help="skip the dequant/transpose timings")
     ap.add_argument("--max-elems", type=int, default=0,
                     help="run a smaller workload of the same kind (profiling cases)")
     args = ap.parse_args()

@@ -16,23 +16,31 @@ constexpr int kBlkElems = FP8Z_BLOCK_ELEMS;
 
 // ------------------------------------------------------------- dequantize
 // "FP8-Flow-MoE" §3.1: D(Q(x)) = Q(x) * s, here value(code) * inv_scale.
-// HBM-bound (1 B read + 4 B written per element): each thread moves 16 codes
-// per iteration with 16-byte loads and four 16-byte streaming stores; the grid
-// is a multiple of the SM count and strides over the buffer.
-__global__ void __launch_bounds__(256) dequant_kernel(const uint4* __restrict__ q,
+// HBM-bound (1 B read + 4 B written per element).  Each thread takes one
+// 32-bit word of codes (4 elements) per step, so a warp reads 128 contiguous
+// bytes of codes and writes 512 contiguous bytes of floats per instruction;
+// four independent words per iteration keep loads in flight.
+__global__ void __launch_bounds__(256) dequant_kernel(const uint32_t* __restrict__ q,
                                                       const float* __restrict__ inv,
-                                                      int64_t nchunks, float4* __restrict__ out) {
+                                                      int64_t nwords, float4* __restrict__ out) {
     const int64_t stride = int64_t(gridDim.x) * blockDim.x;
-    for (int64_t c = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; c < nchunks; c += stride) {
-        const uint4 w = __ldcs(q + c);
-        const float s = __ldg(inv + (c >> 10));         // 1024 chunks of 16 codes per block
-        const uint32_t words[4] = {w.x, w.y, w.z, w.w};
+    for (int64_t w0 = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; w0 < nwords; w0 += 4 * stride) {
+        uint32_t words[4];
+        float s[4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const float2 a = e4m3x2_to_float2(words[j]);
-            const float2 b = e4m3x2_to_float2(words[j] >> 16);
-            __stcs(out + 4 * c + j, make_float4(__fmul_rn(a.x, s), __fmul_rn(a.y, s),
-                                                __fmul_rn(b.x, s), __fmul_rn(b.y, s)));
+        for (int u = 0; u < 4; ++u) {
+            const int64_t w = w0 + u * stride;
+            words[u] = w < nwords ? __ldcs(q + w) : 0u;
+            s[u] = w < nwords ? __ldg(inv + (w >> 12)) : 0.0f;   // 4096 words per block
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int64_t w = w0 + u * stride;
+            if (w >= nwords) break;
+            const float2 a = e4m3x2_to_float2(words[u]);
+            const float2 b = e4m3x2_to_float2(words[u] >> 16);
+            __stcs(out + w, make_float4(__fmul_rn(a.x, s[u]), __fmul_rn(a.y, s[u]),
+                                        __fmul_rn(b.x, s[u]), __fmul_rn(b.y, s[u])));
         }
     }
 }
@@ -150,12 +158,12 @@ extern "C" int fp8z_dequant(const uint8_t* w_fp8, const float* inv_scale, int64_
     int sms = 0;
     const int rc = host::device_sms(&sms);
     if (rc != FP8Z_OK) return rc;
-    const int64_t nchunks = nblk * (kBlkElems / 16);
-    const int64_t want = (nchunks + 255) / 256;
+    const int64_t nwords = nblk * (kBlkElems / 4);
+    const int64_t want = (nwords + 1023) / 1024;
     const int64_t cap = int64_t(sms) * 8;
     const unsigned grid = unsigned(want < cap ? want : cap);
     dequant_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(
-        reinterpret_cast<const uint4*>(w_fp8), inv_scale, nchunks, reinterpret_cast<float4*>(out));
+        reinterpret_cast<const uint32_t*>(w_fp8), inv_scale, nwords, reinterpret_cast<float4*>(out));
     return cudaGetLastError() == cudaSuccess ? FP8Z_OK : FP8Z_ECUDA;
 }
 

@@ -1,0 +1,274 @@
+// fold.cu -- fold / unfold between a parameter's row-major [E, H, W] layout
+// and the flat buffer of contiguous 128x128 blocks (sm_103a).
+//
+// "A ZeRO Optimizer Design for Blockwise FP8 Quantization", "Layout transform
+// (fold/unfold)": fold turns the row-major weight into 128x128 blocks laid out
+// one after another (order e, block row, block col), so the ZeRO-1 optimizer can
+// split it on block boundaries; unfold is the inverse, applied to the gathered
+// FP8 weights after the step.  The quantized dims are zero-padded to multiples
+// of 128 ("Block-wise split").
+//
+// GB300 design: both directions are pure data movement (HBM-bound, 2 x element
+// size per element).  A folded block is one contiguous 16384-element run and in
+// the row-major tensor a 128x128 tile, so each CTA moves whole blocks with the
+// TMA engine: fold = one tiled tensor-map load of the tile (the engine fills the
+// ragged edge with zeros) + one bulk store of the contiguous block; unfold =
+// one bulk load + one tiled tensor-map store (the engine clips at the tensor's
+// edge).  A persistent CTA per SM keeps 192 KB of blocks in flight.  Shapes
+// whose row pitch is not a multiple of 16 bytes (a TMA rule) take a plain
+// kernel instead.
+#include <cstdint>
+#include <cstring>
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include "fp8z.h"
+#include "fp8z_device.cuh"
+#include "fp8z_host.h"
+
+namespace fp8z {
+namespace {
+
+constexpr int kBlk = FP8Z_BLOCK;
+constexpr int kBlkElems = FP8Z_BLOCK_ELEMS;
+
+struct FoldArgs {
+    uint8_t* flat;            // first block of the param in the folded buffer
+    int64_t hb, wb, nblk;     // blocks per row / col of one expert matrix, total
+    int32_t esz;              // element size in bytes (1 or 4)
+    int32_t* dev_status;
+    int64_t timeout_ns;
+};
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y, int z,
+                                            uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+        "l"(map), "r"(x), "r"(y), "r"(z), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, int x, int y, int z, uint32_t src) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(map),
+        "r"(x), "r"(y), "r"(z), "r"(src)
+        : "memory");
+}
+
+__device__ __forceinline__ void bulk_s2g(void* dst, uint32_t src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+// Wait until at most N bulk groups of this thread still read shared memory.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+__device__ __forceinline__ void fence_proxy_async() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Block b of the param -> (x, y, z) of its tile in the row-major tensor.
+__device__ __forceinline__ void tile_coords(const FoldArgs& F, int64_t b, int& x, int& y, int& z) {
+    const int64_t per = F.hb * F.wb;
+    z = int(b / per);
+    const int64_t r = b % per;
+    y = int((r / F.wb) * kBlk);
+    x = int((r % F.wb) * kBlk);
+}
+
+// One thread per CTA drives the copies.  Blocks are dealt round-robin over a
+// persistent grid; each CTA keeps a ring of kRingBytes / block-size buffers,
+// with all but one holding loads in flight while the oldest is written out.
+constexpr int kRingBytes = 192 * 1024;
+
+template <bool kFold>
+__global__ void __launch_bounds__(32) fold_tma_kernel(const __grid_constant__ CUtensorMap map,
+                                                      const FoldArgs F) {
+    extern __shared__ __align__(1024) unsigned char smem[];
+    if (threadIdx.x != 0) return;
+    const uint32_t box = uint32_t(kBlkElems) * F.esz;
+    const int nbuf = int(kRingBytes / box);               // 3 (fp32) or 12 (bytes)
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + size_t(nbuf) * box);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + nbuf);
+    const uint32_t buf0 = smem_addr(smem);
+    const uint32_t bar0 = smem_addr(bars);
+    *abort_flag = 0;
+    for (int i = 0; i < nbuf; ++i) mbar_init(bar0 + 8 * i, 1);
+    fence_mbar_init();
+    const Watchdog wd{abort_flag, F.dev_status, F.timeout_ns};
+
+    const int64_t count = (F.nblk - blockIdx.x + gridDim.x - 1) / gridDim.x;   // grid <= nblk
+    auto blk = [&](int64_t i) { return int64_t(blockIdx.x) + i * gridDim.x; };
+    auto issue_load = [&](int64_t i) {
+        const int s = int(i % nbuf);
+        const uint32_t dst = buf0 + s * box;
+        mbar_arrive_expect_tx(bar0 + 8 * s, box);
+        if (kFold) {
+            int x, y, z;
+            tile_coords(F, blk(i), x, y, z);
+            tma_load_3d(dst, &map, x, y, z, bar0 + 8 * s);
+        } else {
+            bulk_g2s_nohint(dst, F.flat + blk(i) * int64_t(box), box, bar0 + 8 * s);
+        }
+    };
+
+    const int64_t ahead = nbuf - 1;
+    for (int64_t i = 0; i < count && i < ahead; ++i) issue_load(i);
+    for (int64_t i = 0; i < count; ++i) {
+        const int64_t j = i + ahead;
+        if (j < count) {
+            bulk_wait_read<0>();     // block i-1's store has read its buffer (= buffer of block j)
+            issue_load(j);
+        }
+        const int s = int(i % nbuf);
+        if (!mbar_wait_bounded(bar0 + 8 * s, uint32_t((i / nbuf) & 1), wd)) {
+            // let every load still in flight land before the CTA leaves
+            for (int64_t k = i + 1; k < count && k <= j; ++k)
+                mbar_wait_bounded(bar0 + 8 * int(k % nbuf), uint32_t((k / nbuf) & 1), wd, false);
+            bulk_wait_all();
+            return;
+        }
+        fence_proxy_async();
+        const uint32_t src = buf0 + s * box;
+        if (kFold) {
+            bulk_s2g(F.flat + blk(i) * int64_t(box), src, box);
+        } else {
+            int x, y, z;
+            tile_coords(F, blk(i), x, y, z);
+            tma_store_3d(&map, x, y, z, src);
+        }
+        bulk_commit();
+    }
+    bulk_wait_all();
+}
+
+// Plain path for shapes the TMA engine cannot address (row pitch not a
+// multiple of 16 bytes): one CTA per block, rows of the tile read/written by
+// consecutive threads.
+template <bool kFold, typename T>
+__global__ void __launch_bounds__(256) fold_plain_kernel(const T* __restrict__ src, T* __restrict__ dst,
+                                                         int64_t H, int64_t W, int64_t hb, int64_t wb) {
+    const int64_t b = blockIdx.x;
+    const int64_t per = hb * wb;
+    const int64_t e = b / per, r = b % per;
+    const int64_t row0 = (r / wb) * kBlk, col0 = (r % wb) * kBlk;
+    const T* in = kFold ? src : src + b * kBlkElems;
+    T* out = kFold ? dst + b * kBlkElems : dst;
+    for (int i = threadIdx.x; i < kBlkElems; i += blockDim.x) {
+        const int rr = i / kBlk, cc = i % kBlk;
+        const int64_t row = row0 + rr, col = col0 + cc;
+        const bool inside = row < H && col < W;
+        const int64_t g = (e * H + row) * W + col;
+        if (kFold) {
+            out[i] = inside ? in[g] : T(0);
+        } else if (inside) {
+            out[g] = in[i];
+        }
+    }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+int run(bool fold, const void* src, int32_t esz, const fp8z_param_entry* entry, void* dst,
+        int32_t* dev_status, void* stream) {
+    if (!src || !dst || !entry || (esz != 1 && esz != 4)) return FP8Z_EINVAL;
+    const fp8z_param_entry& pe = *entry;
+    if (pe.e < 1 || pe.rows < 1 || pe.cols < 1 || pe.blk_offset < 0) return FP8Z_EINVAL;
+    if (pe.hb != (pe.rows + kBlk - 1) / kBlk || pe.wb != (pe.cols + kBlk - 1) / kBlk) return FP8Z_EINVAL;
+    const int64_t nblk = pe.e * pe.hb * pe.wb;
+    if (nblk > 0x7FFFFFFFLL || pe.e > 0x7FFFFFFFLL) return FP8Z_EINVAL;
+    if (!host::aligned(src, 16) || !host::aligned(dst, 16) || !host::aligned(dev_status, 4))
+        return FP8Z_EALIGN;
+    int sms = 0;
+    int rc = host::device_sms(&sms);
+    if (rc != FP8Z_OK) return rc;
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const uint8_t* flat_c = static_cast<const uint8_t*>(fold ? dst : src) + pe.blk_offset * int64_t(kBlkElems) * esz;
+    uint8_t* flat = const_cast<uint8_t*>(flat_c);
+    void* rowmajor = const_cast<void*>(fold ? src : dst);
+
+    const bool tma_ok = (pe.cols * esz) % 16 == 0 && pe.rows <= 0xFFFFFFFFLL && pe.cols <= 0xFFFFFFFFLL;
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tma_ok ? encode_fn() : nullptr;
+    if (enc) {
+        CUtensorMap map;
+        std::memset(&map, 0, sizeof(map));
+        const cuuint64_t dims[3] = {cuuint64_t(pe.cols), cuuint64_t(pe.rows), cuuint64_t(pe.e)};
+        const cuuint64_t strides[2] = {cuuint64_t(pe.cols * esz), cuuint64_t(pe.rows * pe.cols * esz)};
+        const cuuint32_t boxd[3] = {kBlk, kBlk, 1};
+        const cuuint32_t estr[3] = {1, 1, 1};
+        const CUresult cr = enc(&map, esz == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_UINT8,
+                                3, rowmajor, dims, strides, boxd, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                                CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (cr == CUDA_SUCCESS) {
+            FoldArgs F{flat, pe.hb, pe.wb, nblk, esz, dev_status, host::kDefaultTimeoutNs};
+            const int nbuf = kRingBytes / (kBlkElems * esz);
+            const int smem = kRingBytes + nbuf * 8 + 16;
+            const void* k = fold ? reinterpret_cast<const void*>(&fold_tma_kernel<true>)
+                                 : reinterpret_cast<const void*>(&fold_tma_kernel<false>);
+            rc = host::set_smem_once(k, fold ? 2 : 3, smem);
+            if (rc != FP8Z_OK) return rc;
+            const unsigned grid = unsigned(nblk < sms ? nblk : sms);
+            if (fold)
+                fold_tma_kernel<true><<<grid, 32, smem, st>>>(map, F);
+            else
+                fold_tma_kernel<false><<<grid, 32, smem, st>>>(map, F);
+            return cudaGetLastError() == cudaSuccess ? FP8Z_OK : FP8Z_ECUDA;
+        }
+    }
+    // plain path
+    const unsigned grid = unsigned(nblk);
+    if (esz == 4) {
+        if (fold)
+            fold_plain_kernel<true, float><<<grid, 256, 0, st>>>(static_cast<const float*>(src),
+                                                                 reinterpret_cast<float*>(flat), pe.rows,
+                                                                 pe.cols, pe.hb, pe.wb);
+        else
+            fold_plain_kernel<false, float><<<grid, 256, 0, st>>>(reinterpret_cast<const float*>(flat),
+                                                                  static_cast<float*>(dst), pe.rows, pe.cols,
+                                                                  pe.hb, pe.wb);
+    } else {
+        if (fold)
+            fold_plain_kernel<true, uint8_t><<<grid, 256, 0, st>>>(static_cast<const uint8_t*>(src), flat,
+                                                                   pe.rows, pe.cols, pe.hb, pe.wb);
+        else
+            fold_plain_kernel<false, uint8_t><<<grid, 256, 0, st>>>(flat, static_cast<uint8_t*>(dst),
+                                                                    pe.rows, pe.cols, pe.hb, pe.wb);
+    }
+    return cudaGetLastError() == cudaSuccess ? FP8Z_OK : FP8Z_ECUDA;
+}
+
+}  // namespace
+}  // namespace fp8z
+
+extern "C" int fp8z_fold(const void* src, int32_t elem_bytes, const fp8z_param_entry* entry,
+                         void* blocks, int32_t* dev_status, void* stream) {
+    return fp8z::run(true, src, elem_bytes, entry, blocks, dev_status, stream);
+}
+
+extern "C" int fp8z_unfold(const void* blocks, int32_t elem_bytes, const fp8z_param_entry* entry,
+                           void* dst, int32_t* dev_status, void* stream) {
+    return fp8z::run(false, blocks, elem_bytes, entry, dst, dev_status, stream);
+}

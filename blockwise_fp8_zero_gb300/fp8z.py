@@ -44,8 +44,8 @@ plan_summary_dtype = np.dtype([
 assert param_entry_dtype.itemsize == 64 and block_desc_dtype.itemsize == 20
 
 EXPORTED = ("fp8z_plan_shards", "fp8z_adamw_requant_step", "fp8z_dequant",
-            "fp8z_transpose_fp8", "fp8z_e4m3_encode_bits", "fp8z_watchdog_selftest",
-            "fp8z_status_string")
+            "fp8z_transpose_fp8", "fp8z_fold", "fp8z_unfold", "fp8z_e4m3_encode_bits",
+            "fp8z_watchdog_selftest", "fp8z_status_string")
 
 
 class fp8z_adamw_hparams(ctypes.Structure):
@@ -91,6 +91,8 @@ def lib():
                                               ctypes.POINTER(fp8z_adamw_hparams), P, P]
         L.fp8z_dequant.argtypes = [P, P, i64, P, P]
         L.fp8z_transpose_fp8.argtypes = [P, P, P, P, P, P]
+        L.fp8z_fold.argtypes = [P, i32, P, P, P, P]
+        L.fp8z_unfold.argtypes = [P, i32, P, P, P, P]
         L.fp8z_e4m3_encode_bits.argtypes = [ctypes.c_uint32, i64, P, P]
         L.fp8z_watchdog_selftest.argtypes = [P, i64, P]
         L.fp8z_status_string.argtypes = [ctypes.c_int]
@@ -221,6 +223,39 @@ def fp8z_transpose_fp8(w_fp8, inv_scale, entry, out, inv_scale_t, stream=None):
                                   _dptr(inv_scale_t, torch.float32, "inv_scale_t"),
                                   _stream_handle(stream))
     _check("fp8z_transpose_fp8", rc)
+
+
+def _entry_checks(entry, folded, rowmajor):
+    E, H, W = int(entry["e"]), int(entry["rows"]), int(entry["cols"])
+    nb = E * int(entry["hb"]) * int(entry["wb"])
+    if rowmajor.numel() < E * H * W:
+        raise ValueError("row-major tensor smaller than the param")
+    if folded.numel() < (int(entry["blk_offset"]) + nb) * BLOCK_ELEMS:
+        raise ValueError("folded buffer does not hold the param's blocks")
+    if folded.dtype != rowmajor.dtype or folded.element_size() not in (1, 4):
+        raise ValueError("fold/unfold: both tensors float32 or both uint8")
+
+
+def fp8z_fold(src, entry, blocks, dev_status=None, stream=None):
+    """Row-major [E, rows, cols] -> the param's 128x128 blocks in the folded buffer."""
+    import torch
+    _entry_checks(entry, blocks, src)
+    ent = np.array([entry], dtype=param_entry_dtype)
+    rc = lib().fp8z_fold(_dptr(src, None, "src"), src.element_size(), ent.ctypes.data,
+                         _dptr(blocks, None, "blocks"), _dptr(dev_status, torch.int32, "dev_status"),
+                         _stream_handle(stream))
+    _check("fp8z_fold", rc)
+
+
+def fp8z_unfold(blocks, entry, dst, dev_status=None, stream=None):
+    """The param's 128x128 blocks in the folded buffer -> row-major [E, rows, cols]."""
+    import torch
+    _entry_checks(entry, blocks, dst)
+    ent = np.array([entry], dtype=param_entry_dtype)
+    rc = lib().fp8z_unfold(_dptr(blocks, None, "blocks"), blocks.element_size(), ent.ctypes.data,
+                           _dptr(dst, None, "dst"), _dptr(dev_status, torch.int32, "dev_status"),
+                           _stream_handle(stream))
+    _check("fp8z_unfold", rc)
 
 
 def fp8z_e4m3_encode_bits(first_bits, n, out, stream=None):

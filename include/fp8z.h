@@ -213,6 +213,30 @@ FP8Z_API int fp8z_transpose_fp8(const uint8_t *w_fp8, const float *inv_scale,
                        void *stream);
 
 /*
+ * fp8z_fold / fp8z_unfold -- the layout transform of "A ZeRO Optimizer Design
+ * for Blockwise FP8 Quantization", "Layout transform (fold/unfold)": a
+ * parameter's row-major [e, rows, cols] tensor <-> its run of contiguous
+ * 128x128 blocks in the flat folded buffer (order: expert, block row, block
+ * col; row-major inside a block).  Fold writes the padding of ragged edge
+ * blocks as zeros ("Block-wise split" pads the quantized dims to multiples of
+ * 128); unfold writes only the param's own elements.
+ * elem_bytes: 4 (FP32 params, grads, moments) or 1 (E4M3 codes).
+ * entry: HOST pointer to the param's planner entry (shape, hb, wb, blk_offset).
+ * fold:   src = device [e, rows, cols]; blocks = device base of the folded
+ *         buffer (the param's blocks start at entry->blk_offset).
+ * unfold: blocks = device base of the folded buffer; dst = device [e, rows, cols].
+ * Pointers 16-byte aligned; dev_status as for the step (a wait that gave up).
+ * Uses the TMA engine when cols * elem_bytes is a multiple of 16, a plain
+ * kernel otherwise.  Returns FP8Z_OK / EINVAL / EALIGN / EUNSUPPORTED / ECUDA.
+ * The scale grid needs no unfold: the folded per-block scales are already the
+ * row-major [e, hb, wb] grid.
+ */
+FP8Z_API int fp8z_fold(const void *src, int32_t elem_bytes, const fp8z_param_entry *entry,
+                       void *blocks, int32_t *dev_status, void *stream);
+FP8Z_API int fp8z_unfold(const void *blocks, int32_t elem_bytes, const fp8z_param_entry *entry,
+                         void *dst, int32_t *dev_status, void *stream);
+
+/*
  * fp8z_e4m3_encode_bits -- out[i] = E4M3 code (round to nearest even,
  * saturating, as in the step) of the float whose bit pattern is
  * first_bits + i, for i < n; n a multiple of 4, out device, 16-byte aligned.
