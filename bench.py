@@ -308,7 +308,27 @@ def run_ours(args):
     peak, peak_src = measured_peak()
     traffic = profiled_traffic() if (scaled_note is None and launches_per_step == 1) else None
 
-    aux = None if args.no_aux else time_aux_kernels(w, q, inv, params, dev, stream, peak, g=state["g"])
+    def fused(rm, timed):
+        """The step with fold-on-read / unfold-on-write, on the row-major grad rm."""
+        try:
+            w_row = torch.empty(w.real_elems, dtype=torch.uint8, device=dev)
+        except RuntimeError:
+            return
+        maps = fp8z.fp8z_encode_grad_maps([rm], params, device=dev)
+        hp = fp8z.hparams(**{**hp_kw, "step": t})
+        sh = shards[0]
+        timed(lambda: fp8z.fp8z_adamw_requant_step_rowmajor(
+            state["p"], state["m"], state["v"], maps, w_row, inv, int(sh["blk_begin"]),
+            int(sh["blk_count_real"]), hp, desc, pdev, len(params), w_fp8_t=wt, inv_scale_t=it,
+            dev_status=status, stream=stream), alg_bytes_step, "fp8z_adamw_requant_step_rowmajor")
+        del w_row
+
+    aux = None if (args.no_aux or len(shards) != 1) else time_aux_kernels(
+        w, q, inv, params, dev, stream, peak, g=state["g"], fused=fused)
+    if aux and "fp8z_adamw_requant_step_rowmajor" in aux:
+        aux["unfused_fold_step_unfold_ms"] = round(
+            aux["fp8z_fold_f32"]["ms"] + avg_launch_s * 1e3 + aux["fp8z_unfold_e4m3"]["ms"], 4) \
+            if "fp8z_unfold_e4m3" in aux else None
 
     # ---- end to end through the C ABI with pinned host buffers
     e2e = None if args.no_e2e else run_e2e(args, w, state, q, inv, wt, it, desc, pdev, params,
@@ -344,7 +364,7 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
-def time_aux_kernels(w, q, inv, params, dev, stream, peak, reps=5, g=None):
+def time_aux_kernels(w, q, inv, params, dev, stream, peak, reps=5, g=None, fused=None):
     """Dequantize, the standalone column-major transpose, unfold/fold of the
     FP32 grad and unfold of the E4M3 codes, each timed with CUDA events against
     its algorithmic bytes (dequant: 1 B read + 4 B written per element + 4 B per
@@ -410,6 +430,8 @@ def time_aux_kernels(w, q, inv, params, dev, stream, peak, reps=5, g=None):
         # unfold then fold back: g ends exactly as it started
         timed(lambda: fp8z.fp8z_unfold(g, pe, rm, stream=stream), 8 * E * H * W, "fp8z_unfold_f32")
         timed(lambda: fp8z.fp8z_fold(rm, pe, g, stream=stream), 8 * E * H * W, "fp8z_fold_f32")
+        if fused is not None:
+            fused(rm, timed)
         del rm
         qb = torch.empty(E * H * W, dtype=torch.uint8, device=dev)
         timed(lambda: fp8z.fp8z_unfold(q, pe, qb, stream=stream), 2 * E * H * W, "fp8z_unfold_e4m3")

@@ -36,5 +36,9 @@ int device_sms(int* sms);
 // cudaFuncSetAttribute(MaxDynamicSharedMemorySize) once per (kernel slot, device).
 int set_smem_once(const void* kernel, int slot, int bytes);
 
+// The driver's cuTensorMapEncodeTiled (through the runtime's entry-point
+// query, so the library needs no link against libcuda); nullptr if absent.
+void* tensor_map_encoder();
+
 }  // namespace host
 }  // namespace fp8z

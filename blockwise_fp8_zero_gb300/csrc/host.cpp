@@ -88,6 +88,20 @@ int set_smem_once(const void* kernel, int slot, int bytes) {
     return FP8Z_OK;
 }
 
+void* tensor_map_encoder() {
+    static std::atomic<void*> fn{nullptr};
+    void* f = fn.load(std::memory_order_acquire);
+    if (!f) {
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return nullptr;
+        fn.store(f, std::memory_order_release);
+    }
+    return f;
+}
+
 }  // namespace host
 }  // namespace fp8z
 

@@ -25,6 +25,8 @@
 #include <cstdint>
 #include <cstring>
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include "fp8z.h"
@@ -37,8 +39,8 @@ namespace {
 // Build-time shape of the pipeline.  The defaults won a sweep on GB300 at
 // 6e9 elements (28.0 ms per step): a deeper ring is faster (4 and 5 stages
 // lose 2-6 %), plain bulk loads beat the L2 evict-first hint (+1.5 %),
-// streaming stores of the FP32 outputs help once the loads are plain, loading
-// the next block's descriptor early helps a little (+0.2 %).  Losers dropped
+// streaming stores of the FP32 outputs help once the loads are plain.  Losers
+// dropped
 // from the code: L2 prefetch ahead of the ring (-35 %), one contiguous block
 // range per CTA (-2.5 %), streaming stores of the E4M3 bytes (-2.5 %), two
 // rows per warp per stage with 3 stages (-10 %).
@@ -46,8 +48,6 @@ namespace {
 //   FP8Z_ROWS_PER_WARP    block rows each consumer warp takes per stage
 //   FP8Z_STORE_STREAMING  1: p', m', v' stored with the streaming (.cs) hint
 //   FP8Z_LOAD_EVICT_FIRST 1: bulk loads carry an L2 evict-first policy
-//   FP8Z_PREFETCH_NEXT    1: a block's descriptor and copy target are loaded
-//                         one block ahead of their use
 #ifndef FP8Z_RING
 #define FP8Z_RING 6
 #endif
@@ -59,9 +59,6 @@ namespace {
 #endif
 #ifndef FP8Z_LOAD_EVICT_FIRST
 #define FP8Z_LOAD_EVICT_FIRST 0
-#endif
-#ifndef FP8Z_PREFETCH_NEXT
-#define FP8Z_PREFETCH_NEXT 1
 #endif
 
 constexpr int kBlk = FP8Z_BLOCK;
@@ -83,7 +80,9 @@ static_assert(kKeep * kConsumers * 4 == kBlkElems, "consumer layout");
 constexpr size_t kRingBytes = size_t(kRing) * kStageBytes;
 constexpr size_t kTileBytes = kBlkElems;                 // 16 KB byte tile
 constexpr size_t kAmaxBytes = 2 * kConsumerWarps * sizeof(float);
-constexpr size_t kBarOffset = kRingBytes + kTileBytes + kAmaxBytes;
+constexpr size_t kCtxOffset = kRingBytes + kTileBytes + kAmaxBytes;
+constexpr size_t kCtxBytes = 2 * 80;                     // two BlockCtx slots
+constexpr size_t kBarOffset = kCtxOffset + kCtxBytes;
 constexpr int kNumBars = 2 * kRing + 2;
 constexpr size_t kSmemBytes = kBarOffset + kNumBars * 8 + 16;
 
@@ -104,6 +103,10 @@ struct StepArgs {
     int64_t inv_scale_t_count;
     int32_t* dev_status;
     int64_t timeout_ns;
+    // row-major variant: per-param grad tensor maps, whole-param E4M3 buffer
+    const CUtensorMap* g_maps;
+    uint8_t* w_row;
+    int64_t w_row_bytes;
     float beta1, beta2, omb1, omb2, eps, step_size, rs_bc2, decay, lr_wd;
     float fp8_max, min_scale, min_scale_pow2;
     int32_t scale_mode, decay_mode;
@@ -178,10 +181,23 @@ struct BlockInfo {
     int param, e, brow, bcol;
 };
 
-// Where a block's column-major copy goes (loaded one block ahead).
+// Where a block's row-major / column-major bytes go.
 struct ParamInfo {
     int64_t e, H, W, hb, wb, t_off, ts_off;
 };
+
+// A block's descriptor and param entry, fetched from global memory by the
+// producer one block ahead and handed to the consumers through shared memory
+// (written before the block's first stage is armed; the mbarrier's
+// release/acquire orders it).  Two slots, by block parity: the producer can
+// refill a slot only after every consumer warp has released a stage of the
+// following block, i.e. has finished with the block that used it.
+struct BlockCtx {
+    BlockInfo bi;        // 24 bytes
+    ParamInfo pi;        // 56 bytes
+};
+static_assert(sizeof(BlockCtx) == 80, "context slot size");
+static_assert(kRing <= kStagesPerBlock, "context slots need the producer within one block");
 
 __device__ __forceinline__ BlockInfo load_desc(const StepArgs& A, int64_t blk) {
     BlockInfo bi{kBlk, kBlk, -1, 0, 0, 0};
@@ -200,7 +216,7 @@ __device__ __forceinline__ BlockInfo load_desc(const StepArgs& A, int64_t blk) {
 
 __device__ __forceinline__ ParamInfo load_param(const StepArgs& A, const BlockInfo& bi) {
     ParamInfo pi{0, 0, 0, 0, 0, 0, 0};
-    if (A.w_fp8_t != nullptr && bi.param >= 0 && bi.param < A.nparams) {
+    if ((A.w_fp8_t != nullptr || A.w_row != nullptr) && bi.param >= 0 && bi.param < A.nparams) {
         const fp8z_param_entry* pe = A.params + bi.param;
         pi.e = __ldg(&pe->e);
         pi.H = __ldg(&pe->rows);
@@ -238,6 +254,42 @@ __device__ __forceinline__ BlockSched block_sched(int64_t blk_begin, int64_t nbl
                       (nblk - blockIdx.x + gridDim.x - 1) / gridDim.x};
 }
 
+// Does block bi of param pi have a destination inside a buffer of `bytes`
+// bytes (and, for the transposed grid, `scales` entries)?  A descriptor that
+// disagrees with the param table is rejected, so no write can leave the buffer.
+__device__ __forceinline__ bool dest_ok(const StepArgs& A, const BlockInfo& bi, const ParamInfo& pi,
+                                        int64_t bytes, int64_t scales) {
+    const int64_t H = pi.H, W = pi.W;
+    return bi.param >= 0 && bi.param < A.nparams && bi.e >= 0 && bi.e < pi.e && bi.brow >= 0 &&
+           bi.brow < pi.hb && bi.bcol >= 0 && bi.bcol < pi.wb &&
+           bi.vr == imin64(kBlk, H - bi.brow * int64_t(kBlk)) &&
+           bi.vc == imin64(kBlk, W - bi.bcol * int64_t(kBlk)) && pi.t_off >= 0 &&
+           pi.t_off + (bi.e + 1) * H * W <= bytes &&
+           (scales < 0 || (pi.ts_off >= 0 && pi.ts_off + (bi.e + 1) * pi.hb * pi.wb <= scales));
+}
+
+// Row-major E4M3 write of one block into the whole-param buffer ("Summary"
+// of the ZeRO design page: the FP8 params are unfolded back to their 2-D/3-D
+// shape; here the unfold happens on the way out).  Row r of the block is 128
+// contiguous bytes of row brow*128 + r of the param.
+__device__ __forceinline__ void store_rowmajor(const StepArgs& A, const BlockInfo& bi, const ParamInfo& pi,
+                                               const uint32_t (&words)[kKeep], int warp, int col) {
+    const int64_t H = pi.H, W = pi.W;
+    const int64_t base = pi.t_off + bi.e * H * W + int64_t(bi.brow) * kBlk * W + int64_t(bi.bcol) * kBlk;
+    const bool aligned = ((pi.t_off + bi.e * H * W) | W) % 4 == 0;
+#pragma unroll
+    for (int k = 0; k < kKeep; ++k) {
+        const int row = k * kConsumerWarps + warp;
+        if (row >= bi.vr || col >= bi.vc) continue;
+        uint8_t* dst = A.w_row + base + int64_t(row) * W + col;
+        if (aligned && col + 3 < bi.vc) {
+            store_word(dst, words[k]);
+        } else {
+            for (int b = 0; b < 4 && col + b < bi.vc; ++b) dst[b] = uint8_t(words[k] >> (8 * b));
+        }
+    }
+}
+
 // Column-major copy of one block: the quantized words go through a swizzled
 // shared tile; each warp then writes four output rows per pass, 128
 // contiguous bytes per warp store.  Returns false when a wait gave up.
@@ -247,13 +299,7 @@ __device__ __forceinline__ bool column_major_copy(const StepArgs& A, const Block
                                                   uint32_t& tile_phase, const Watchdog& wd,
                                                   int tid, int warp, int lane) {
     const int64_t H = pi.H, W = pi.W;
-    const bool ok = bi.param < A.nparams && bi.e >= 0 && bi.e < pi.e && bi.brow >= 0 &&
-                    bi.brow < pi.hb && bi.bcol >= 0 && bi.bcol < pi.wb &&
-                    bi.vr == imin64(kBlk, H - bi.brow * int64_t(kBlk)) &&
-                    bi.vc == imin64(kBlk, W - bi.bcol * int64_t(kBlk)) && pi.t_off >= 0 &&
-                    pi.ts_off >= 0 && pi.t_off + (bi.e + 1) * H * W <= A.w_fp8_t_bytes &&
-                    pi.ts_off + (bi.e + 1) * pi.hb * pi.wb <= A.inv_scale_t_count;
-    if (!ok) {
+    if (!dest_ok(A, bi, pi, A.w_fp8_t_bytes, A.inv_scale_t_count)) {
         if (tid == 0) report_status(A.dev_status, FP8Z_EINVAL);
         return true;
     }
@@ -295,11 +341,13 @@ __device__ __forceinline__ bool column_major_copy(const StepArgs& A, const Block
     return true;
 }
 
+template <bool kRowMajor>
 __global__ void __launch_bounds__(kThreads, 1) fp8z_step_kernel(const StepArgs A) {
     extern __shared__ __align__(1024) unsigned char smem[];
     float* ring = reinterpret_cast<float*>(smem);
     uint32_t* tile = reinterpret_cast<uint32_t*>(smem + kRingBytes);
     float* amax_x = reinterpret_cast<float*>(smem + kRingBytes + kTileBytes);
+    BlockCtx* ctx = reinterpret_cast<BlockCtx*>(smem + kCtxOffset);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kBarOffset);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + kNumBars);
 
@@ -338,21 +386,43 @@ __global__ void __launch_bounds__(kThreads, 1) fp8z_step_kernel(const StepArgs A
         int slot = 0;
         uint32_t phase = 0;
         int64_t issued = 0;
+        BlockInfo pbi = load_desc(A, sched.blk(0));
+        ctx[0].bi = pbi;
+        ctx[0].pi = load_param(A, pbi);
         for (int64_t i = 0; i < nmine; ++i) {
             const size_t base = size_t(sched.blk(i)) * kBlkElems;
+            const bool has_next = i + 1 < nmine;
+            // the next block's descriptor now, its param entry mid-block: both
+            // have landed by the time the next block's context is written
+            BlockInfo pnext = pbi;
+            ParamInfo pinext{0, 0, 0, 0, 0, 0, 0};
+            if (has_next) pnext = load_desc(A, sched.blk(i + 1));
+            // row-major grad: the stage is rows [k*16, k*16+16) of the block's
+            // 128x128 tile of the param's [E,H,W] grad, zero past its edge
+            const bool gmap_ok = kRowMajor && pbi.param >= 0 && pbi.param < A.nparams;
             for (int k = 0; k < kStagesPerBlock; ++k) {
+                if (has_next && k == kStagesPerBlock / 2) pinext = load_param(A, pnext);
                 if (!mbar_wait_bounded(empty0 + 8 * slot, phase ^ 1, wd)) goto drain;
                 const uint32_t full = full0 + 8 * slot;
-                mbar_arrive_expect_tx(full, kStageBytes);
+                mbar_arrive_expect_tx(full, (kRowMajor && !gmap_ok) ? 3 * kTensorStageBytes : kStageBytes);
                 const uint32_t dst = ring0 + slot * kStageBytes;
                 const size_t off = base + size_t(k) * kStageElems;
+                if (kRowMajor) {
+                    if (gmap_ok)
+                        tma_load_3d(dst, A.g_maps + pbi.param, pbi.bcol * kBlk,
+                                    pbi.brow * kBlk + k * kStageRows, pbi.e, full);
+                } else {
 #if FP8Z_LOAD_EVICT_FIRST
-                bulk_g2s(dst + 0 * kTensorStageBytes, A.g + off, kTensorStageBytes, full, pol);
+                    bulk_g2s(dst + 0 * kTensorStageBytes, A.g + off, kTensorStageBytes, full, pol);
+#else
+                    bulk_g2s_nohint(dst + 0 * kTensorStageBytes, A.g + off, kTensorStageBytes, full);
+#endif
+                }
+#if FP8Z_LOAD_EVICT_FIRST
                 bulk_g2s(dst + 1 * kTensorStageBytes, A.p + off, kTensorStageBytes, full, pol);
                 bulk_g2s(dst + 2 * kTensorStageBytes, A.m + off, kTensorStageBytes, full, pol);
                 bulk_g2s(dst + 3 * kTensorStageBytes, A.v + off, kTensorStageBytes, full, pol);
 #else
-                bulk_g2s_nohint(dst + 0 * kTensorStageBytes, A.g + off, kTensorStageBytes, full);
                 bulk_g2s_nohint(dst + 1 * kTensorStageBytes, A.p + off, kTensorStageBytes, full);
                 bulk_g2s_nohint(dst + 2 * kTensorStageBytes, A.m + off, kTensorStageBytes, full);
                 bulk_g2s_nohint(dst + 3 * kTensorStageBytes, A.v + off, kTensorStageBytes, full);
@@ -360,6 +430,11 @@ __global__ void __launch_bounds__(kThreads, 1) fp8z_step_kernel(const StepArgs A
                 ++issued;
                 if (++slot == kRing) { slot = 0; phase ^= 1; }
             }
+            if (has_next) {
+                ctx[(i + 1) & 1].bi = pnext;
+                ctx[(i + 1) & 1].pi = pinext;
+            }
+            pbi = pnext;
         }
         return;
     drain:
@@ -381,27 +456,24 @@ __global__ void __launch_bounds__(kThreads, 1) fp8z_step_kernel(const StepArgs A
     int slot = 0;
     uint32_t phase = 0;
     uint32_t tile_phase = 0;
-#if FP8Z_PREFETCH_NEXT
-    BlockInfo bi = load_desc(A, sched.blk(0));
-#endif
 
     for (int64_t i = 0; i < nmine; ++i) {
         const int64_t blk = sched.blk(i);
         const size_t base = size_t(blk) * kBlkElems;
-#if FP8Z_PREFETCH_NEXT
-        // descriptor of the next block and this block's copy target, issued a
-        // block ahead of their use so their latency is hidden
-        const BlockInfo bnext = (i + 1 < nmine) ? load_desc(A, sched.blk(i + 1)) : bi;
-        const ParamInfo pi = load_param(A, bi);
-#else
-        const BlockInfo bi = load_desc(A, blk);
-#endif
+        const BlockCtx* c = ctx + (i & 1);
+        int vr = kBlk, vc = kBlk;
+        bool g_ok = true;
 
         float4 keep[kKeep];
         float lmax = 0.0f;
 #pragma unroll
         for (int k = 0; k < kStagesPerBlock; ++k) {
             if (!mbar_wait_bounded(full0 + 8 * slot, phase, wd)) return;
+            if (k == 0) {        // the block's context is visible once its first stage is
+                vr = c->bi.vr;
+                vc = c->bi.vc;
+                g_ok = !kRowMajor || (c->bi.param >= 0 && c->bi.param < A.nparams);
+            }
             const float* st = ring + size_t(slot) * (kStageBytes / 4);
             float4 g4[kRowsPerWarp], p4[kRowsPerWarp], m4[kRowsPerWarp], v4[kRowsPerWarp];
 #pragma unroll
@@ -415,6 +487,10 @@ __global__ void __launch_bounds__(kThreads, 1) fp8z_step_kernel(const StepArgs A
             __syncwarp();
             if (lane == 0) mbar_arrive(empty0 + 8 * slot);
             if (++slot == kRing) { slot = 0; phase ^= 1; }
+            if (kRowMajor && !g_ok) {
+#pragma unroll
+                for (int r = 0; r < kRowsPerWarp; ++r) g4[r] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
 
 #pragma unroll
             for (int r = 0; r < kRowsPerWarp; ++r) {
@@ -426,12 +502,12 @@ __global__ void __launch_bounds__(kThreads, 1) fp8z_step_kernel(const StepArgs A
 
                 const int kk = k * kRowsPerWarp + r;
                 const int row = kk * kConsumerWarps + warp;
-                if (row >= bi.vr || col + 3 >= bi.vc) {     // padding of a ragged edge block
-                    const bool rv = row < bi.vr;
-                    if (!(rv && col + 0 < bi.vc)) { p1.x = 0.f; m1.x = 0.f; v1.x = 0.f; }
-                    if (!(rv && col + 1 < bi.vc)) { p1.y = 0.f; m1.y = 0.f; v1.y = 0.f; }
-                    if (!(rv && col + 2 < bi.vc)) { p1.z = 0.f; m1.z = 0.f; v1.z = 0.f; }
-                    if (!(rv && col + 3 < bi.vc)) { p1.w = 0.f; m1.w = 0.f; v1.w = 0.f; }
+                if (row >= vr || col + 3 >= vc) {           // padding of a ragged edge block
+                    const bool rv = row < vr;
+                    if (!(rv && col + 0 < vc)) { p1.x = 0.f; m1.x = 0.f; v1.x = 0.f; }
+                    if (!(rv && col + 1 < vc)) { p1.y = 0.f; m1.y = 0.f; v1.y = 0.f; }
+                    if (!(rv && col + 2 < vc)) { p1.z = 0.f; m1.z = 0.f; v1.z = 0.f; }
+                    if (!(rv && col + 3 < vc)) { p1.w = 0.f; m1.w = 0.f; v1.w = 0.f; }
                 }
                 const size_t off = base + size_t(row) * kBlk + col;
                 store4(A.p + off, p1);
@@ -459,29 +535,33 @@ __global__ void __launch_bounds__(kThreads, 1) fp8z_step_kernel(const StepArgs A
         const float inv = __fdiv_rn(1.0f, s);
         if (tid == 0) A.inv_scale[blk] = inv;
 
-        // ---- quantize the kept p' and store the row-major E4M3 block
+        // ---- quantize the kept p' and store the E4M3 block
         uint32_t words[kKeep];
 #pragma unroll
         for (int k = 0; k < kKeep; ++k) {
             const float4 x = keep[k];
             words[k] = pack_e4m3x4(__fmul_rn(x.x, s), __fmul_rn(x.y, s), __fmul_rn(x.z, s),
                                    __fmul_rn(x.w, s));
-            const int row = k * kConsumerWarps + warp;
-            store_word(A.w_fp8 + base + size_t(row) * kBlk + col, words[k]);
+            if (!kRowMajor) {
+                const int row = k * kConsumerWarps + warp;
+                store_word(A.w_fp8 + base + size_t(row) * kBlk + col, words[k]);
+            }
+        }
+        const BlockInfo bi = c->bi;
+        const ParamInfo pi = c->pi;
+        if (kRowMajor && bi.param >= 0) {
+            if (dest_ok(A, bi, pi, A.w_row_bytes, -1))
+                store_rowmajor(A, bi, pi, words, warp, col);
+            else if (tid == 0)
+                report_status(A.dev_status, FP8Z_EINVAL);
         }
 
         // ---- optional column-major copy of the param + transposed scale grid
         if (transposed && bi.param >= 0) {
-#if !FP8Z_PREFETCH_NEXT
-            const ParamInfo pi = load_param(A, bi);
-#endif
             if (!column_major_copy(A, bi, pi, words, inv, tile, tile_bar, tile_phase, wd, tid, warp,
                                    lane))
                 return;
         }
-#if FP8Z_PREFETCH_NEXT
-        bi = bnext;
-#endif
     }
 }
 
@@ -489,6 +569,68 @@ __global__ void __launch_bounds__(kThreads, 1) fp8z_step_kernel(const StepArgs A
 }  // namespace fp8z
 
 using namespace fp8z;
+
+namespace {
+
+// Checks shared by both entry points; fills the common fields of A.
+int prepare(StepArgs& A, float* p, float* m, float* v, float* inv_scale, int64_t capacity_blocks,
+            int64_t blk_begin, int64_t nblk, const fp8z_block_desc* desc,
+            const fp8z_param_entry* params, int32_t nparams, uint8_t* w_fp8_t,
+            int64_t w_fp8_t_bytes, float* inv_scale_t, int64_t inv_scale_t_count,
+            const fp8z_adamw_hparams* hp, int32_t* dev_status) {
+    if (!p || !m || !v || !inv_scale || !hp) return FP8Z_EINVAL;
+    if (capacity_blocks < 0 || blk_begin < 0 || nblk < 0) return FP8Z_EINVAL;
+    if (capacity_blocks > (INT64_MAX / kBlkElems) / 4) return FP8Z_EINVAL;
+    if (blk_begin > capacity_blocks || nblk > capacity_blocks - blk_begin) return FP8Z_ENOSPACE;
+    const bool want_t = (w_fp8_t != nullptr) || (inv_scale_t != nullptr);
+    if (want_t && (!w_fp8_t || !inv_scale_t || !desc || !params || nparams <= 0 ||
+                   w_fp8_t_bytes < 0 || inv_scale_t_count < 0))
+        return FP8Z_EINVAL;
+    if (!host::aligned(p, 16) || !host::aligned(m, 16) || !host::aligned(v, 16) ||
+        !host::aligned(inv_scale, 4) || !host::aligned(desc, 4) || !host::aligned(params, 8) ||
+        !host::aligned(w_fp8_t, 16) || !host::aligned(inv_scale_t, 4) || !host::aligned(dev_status, 4))
+        return FP8Z_EALIGN;
+    if (!host::hparams_valid(*hp)) return FP8Z_EINVAL;
+    std::memset(&A, 0, sizeof(A));
+    A.p = p; A.m = m; A.v = v;
+    A.inv_scale = inv_scale;
+    A.blk_begin = blk_begin; A.nblk = nblk;
+    A.desc = desc;
+    A.params = params;
+    A.nparams = params ? nparams : 0;
+    A.w_fp8_t = want_t ? w_fp8_t : nullptr;
+    A.w_fp8_t_bytes = w_fp8_t_bytes;
+    A.inv_scale_t = want_t ? inv_scale_t : nullptr;
+    A.inv_scale_t_count = inv_scale_t_count;
+    A.dev_status = dev_status;
+    A.timeout_ns = host::kDefaultTimeoutNs;
+    const host::AdamwScalars sc = host::adamw_scalars(*hp);
+    A.beta1 = sc.beta1; A.beta2 = sc.beta2; A.omb1 = sc.omb1; A.omb2 = sc.omb2;
+    A.eps = sc.eps; A.step_size = sc.step_size; A.rs_bc2 = sc.rs_bc2;
+    A.decay = sc.decay; A.lr_wd = sc.lr_wd;
+    A.fp8_max = hp->fp8_max; A.min_scale = hp->min_scale;
+    A.min_scale_pow2 = host::pow2_at_least(hp->min_scale);
+    A.scale_mode = hp->scale_mode; A.decay_mode = hp->decay_mode;
+    return FP8Z_OK;
+}
+
+template <bool kRowMajor>
+int launch(const StepArgs& A, void* stream) {
+    if (A.nblk == 0) return FP8Z_OK;
+    int sms = 0;
+    int rc = host::device_sms(&sms);
+    if (rc != FP8Z_OK) return rc;
+    static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+    rc = host::set_smem_once(reinterpret_cast<const void*>(&fp8z_step_kernel<kRowMajor>), kRowMajor ? 1 : 0,
+                             int(kSmemBytes));
+    if (rc != FP8Z_OK) return rc;
+    const int64_t grid = A.nblk < sms ? A.nblk : sms;
+    fp8z_step_kernel<kRowMajor><<<dim3(unsigned(grid)), dim3(kThreads), kSmemBytes,
+                                  static_cast<cudaStream_t>(stream)>>>(A);
+    return cudaGetLastError() == cudaSuccess ? FP8Z_OK : FP8Z_ECUDA;
+}
+
+}  // namespace
 
 extern "C" int fp8z_adamw_requant_step(float* p, const float* g, float* m, float* v,
                                        uint8_t* w_fp8, float* inv_scale, int64_t capacity_blocks,
@@ -499,53 +641,63 @@ extern "C" int fp8z_adamw_requant_step(float* p, const float* g, float* m, float
                                        float* inv_scale_t, int64_t inv_scale_t_count,
                                        const fp8z_adamw_hparams* hp, int32_t* dev_status,
                                        void* stream) {
-    if (!p || !g || !m || !v || !w_fp8 || !inv_scale || !hp) return FP8Z_EINVAL;
-    if (capacity_blocks < 0 || blk_begin < 0 || nblk < 0) return FP8Z_EINVAL;
-    if (capacity_blocks > (INT64_MAX / kBlkElems) / 4) return FP8Z_EINVAL;
-    if (blk_begin > capacity_blocks || nblk > capacity_blocks - blk_begin) return FP8Z_ENOSPACE;
+    if (!g || !w_fp8) return FP8Z_EINVAL;
+    if (!host::aligned(g, 16) || !host::aligned(w_fp8, 16)) return FP8Z_EALIGN;
     const bool want_t = (w_fp8_t != nullptr) || (inv_scale_t != nullptr);
-    if (want_t && (!w_fp8_t || !inv_scale_t || !desc || !params || nparams <= 0 ||
-                   w_fp8_t_bytes < 0 || inv_scale_t_count < 0))
-        return FP8Z_EINVAL;
-    if (!host::aligned(p, 16) || !host::aligned(g, 16) || !host::aligned(m, 16) ||
-        !host::aligned(v, 16) || !host::aligned(w_fp8, 16) || !host::aligned(inv_scale, 4) ||
-        !host::aligned(desc, 4) || !host::aligned(params, 8) || !host::aligned(w_fp8_t, 16) ||
-        !host::aligned(inv_scale_t, 4) || !host::aligned(dev_status, 4))
-        return FP8Z_EALIGN;
-    if (!host::hparams_valid(*hp)) return FP8Z_EINVAL;
-    if (nblk == 0) return FP8Z_OK;
-
-    int sms = 0;
-    int rc = host::device_sms(&sms);
-    if (rc != FP8Z_OK) return rc;
-    static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
-    rc = host::set_smem_once(reinterpret_cast<const void*>(&fp8z_step_kernel), 0, int(kSmemBytes));
-    if (rc != FP8Z_OK) return rc;
-
     StepArgs A;
-    std::memset(&A, 0, sizeof(A));
-    A.p = p; A.g = g; A.m = m; A.v = v;
-    A.w_fp8 = w_fp8; A.inv_scale = inv_scale;
-    A.blk_begin = blk_begin; A.nblk = nblk;
-    A.desc = desc;
-    A.params = want_t ? params : nullptr;
-    A.nparams = nparams;
-    A.w_fp8_t = want_t ? w_fp8_t : nullptr;
-    A.w_fp8_t_bytes = w_fp8_t_bytes;
-    A.inv_scale_t = want_t ? inv_scale_t : nullptr;
-    A.inv_scale_t_count = inv_scale_t_count;
-    A.dev_status = dev_status;
-    A.timeout_ns = host::kDefaultTimeoutNs;
-    host::AdamwScalars sc = host::adamw_scalars(*hp);
-    A.beta1 = sc.beta1; A.beta2 = sc.beta2; A.omb1 = sc.omb1; A.omb2 = sc.omb2;
-    A.eps = sc.eps; A.step_size = sc.step_size; A.rs_bc2 = sc.rs_bc2;
-    A.decay = sc.decay; A.lr_wd = sc.lr_wd;
-    A.fp8_max = hp->fp8_max; A.min_scale = hp->min_scale;
-    A.min_scale_pow2 = host::pow2_at_least(hp->min_scale);
-    A.scale_mode = hp->scale_mode; A.decay_mode = hp->decay_mode;
+    const int rc = prepare(A, p, m, v, inv_scale, capacity_blocks, blk_begin, nblk, desc,
+                           want_t ? params : nullptr, nparams, w_fp8_t, w_fp8_t_bytes, inv_scale_t,
+                           inv_scale_t_count, hp, dev_status);
+    if (rc != FP8Z_OK) return rc;
+    A.g = g;
+    A.w_fp8 = w_fp8;
+    return launch<false>(A, stream);
+}
 
-    const int64_t grid = nblk < sms ? nblk : sms;
-    fp8z_step_kernel<<<dim3(unsigned(grid)), dim3(kThreads), kSmemBytes,
-                       static_cast<cudaStream_t>(stream)>>>(A);
-    return cudaGetLastError() == cudaSuccess ? FP8Z_OK : FP8Z_ECUDA;
+extern "C" int fp8z_adamw_requant_step_rowmajor(float* p, float* m, float* v, const void* g_maps,
+                                                uint8_t* w_row, int64_t w_row_bytes, float* inv_scale,
+                                                int64_t capacity_blocks, int64_t blk_begin, int64_t nblk,
+                                                const fp8z_block_desc* desc,
+                                                const fp8z_param_entry* params, int32_t nparams,
+                                                uint8_t* w_fp8_t, int64_t w_fp8_t_bytes,
+                                                float* inv_scale_t, int64_t inv_scale_t_count,
+                                                const fp8z_adamw_hparams* hp, int32_t* dev_status,
+                                                void* stream) {
+    if (!g_maps || !w_row || !desc || !params || nparams <= 0 || w_row_bytes < 0) return FP8Z_EINVAL;
+    if (!host::aligned(g_maps, 64) || !host::aligned(w_row, 16)) return FP8Z_EALIGN;
+    StepArgs A;
+    const int rc = prepare(A, p, m, v, inv_scale, capacity_blocks, blk_begin, nblk, desc, params,
+                           nparams, w_fp8_t, w_fp8_t_bytes, inv_scale_t, inv_scale_t_count, hp,
+                           dev_status);
+    if (rc != FP8Z_OK) return rc;
+    A.g_maps = static_cast<const CUtensorMap*>(g_maps);
+    A.w_row = w_row;
+    A.w_row_bytes = w_row_bytes;
+    return launch<true>(A, stream);
+}
+
+extern "C" int fp8z_encode_grad_maps(const void* const* g_ptrs, const fp8z_param_entry* params,
+                                     int32_t nparams, void* maps_out) {
+    if (!g_ptrs || !params || !maps_out || nparams <= 0) return FP8Z_EINVAL;
+    if (!host::aligned(maps_out, 64)) return FP8Z_EALIGN;
+    auto enc = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(host::tensor_map_encoder());
+    if (!enc) return FP8Z_ECUDA;
+    CUtensorMap* maps = static_cast<CUtensorMap*>(maps_out);
+    for (int32_t i = 0; i < nparams; ++i) {
+        const fp8z_param_entry& pe = params[i];
+        if (!g_ptrs[i] || pe.e < 1 || pe.rows < 1 || pe.cols < 1 || pe.e > 0x7FFFFFFFLL ||
+            pe.rows > 0xFFFFFFFFLL || pe.cols > 0xFFFFFFFFLL)
+            return FP8Z_EINVAL;
+        if (!host::aligned(g_ptrs[i], 16) || (pe.cols * 4) % 16 != 0) return FP8Z_EALIGN;
+        const cuuint64_t dims[3] = {cuuint64_t(pe.cols), cuuint64_t(pe.rows), cuuint64_t(pe.e)};
+        const cuuint64_t strides[2] = {cuuint64_t(pe.cols * 4), cuuint64_t(pe.rows * pe.cols * 4)};
+        const cuuint32_t boxd[3] = {kBlk, kStageRows, 1};
+        const cuuint32_t estr[3] = {1, 1, 1};
+        std::memset(&maps[i], 0, sizeof(CUtensorMap));
+        if (enc(&maps[i], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(g_ptrs[i]), dims, strides,
+                boxd, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return FP8Z_EINVAL;
+    }
+    return FP8Z_OK;
 }

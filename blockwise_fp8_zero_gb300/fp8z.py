@@ -43,7 +43,8 @@ plan_summary_dtype = np.dtype([
 ])
 assert param_entry_dtype.itemsize == 64 and block_desc_dtype.itemsize == 20
 
-EXPORTED = ("fp8z_plan_shards", "fp8z_adamw_requant_step", "fp8z_dequant",
+EXPORTED = ("fp8z_plan_shards", "fp8z_adamw_requant_step", "fp8z_adamw_requant_step_rowmajor",
+            "fp8z_encode_grad_maps", "fp8z_dequant",
             "fp8z_transpose_fp8", "fp8z_fold", "fp8z_unfold", "fp8z_e4m3_encode_bits",
             "fp8z_watchdog_selftest", "fp8z_status_string")
 
@@ -89,6 +90,10 @@ def lib():
         L.fp8z_adamw_requant_step.argtypes = [P, P, P, P, P, P, i64, i64, i64, P, P, i32,
                                               P, i64, P, i64,
                                               ctypes.POINTER(fp8z_adamw_hparams), P, P]
+        L.fp8z_adamw_requant_step_rowmajor.argtypes = [P, P, P, P, P, i64, P, i64, i64, i64, P, P, i32,
+                                                       P, i64, P, i64,
+                                                       ctypes.POINTER(fp8z_adamw_hparams), P, P]
+        L.fp8z_encode_grad_maps.argtypes = [P, P, i32, P]
         L.fp8z_dequant.argtypes = [P, P, i64, P, P]
         L.fp8z_transpose_fp8.argtypes = [P, P, P, P, P, P]
         L.fp8z_fold.argtypes = [P, i32, P, P, P, P]
@@ -194,6 +199,53 @@ def fp8z_adamw_requant_step(p, g, m, v, w_fp8, inv_scale, blk_begin, nblk, hp,
         0 if inv_scale_t is None else inv_scale_t.numel(),
         ctypes.byref(hp), _dptr(dev_status, torch.int32, "dev_status"), _stream_handle(stream))
     _check("fp8z_adamw_requant_step", rc)
+
+
+def fp8z_encode_grad_maps(grads, params, device="cuda"):
+    """Tensor maps over each param's row-major FP32 grad (torch CUDA tensors of
+    shape [e, rows, cols] or flat), returned as a CUDA byte tensor to pass as
+    g_maps.  The grads must stay alive while the maps are used."""
+    import torch
+    n = len(params)
+    if len(grads) != n:
+        raise ValueError("one grad per param")
+    for gt, pe in zip(grads, params):
+        if gt.dtype != torch.float32 or gt.numel() < int(pe["e"]) * int(pe["rows"]) * int(pe["cols"]):
+            raise ValueError("grad must be float32 and hold the whole param")
+    ptrs = (ctypes.c_void_p * n)(*[_dptr(gt, torch.float32, "grad") for gt in grads])
+    raw = np.zeros(n * 128 + 64, dtype=np.uint8)
+    off = (-raw.ctypes.data) % 64
+    host = raw[off:off + n * 128]
+    ent = np.ascontiguousarray(params, dtype=param_entry_dtype)
+    rc = lib().fp8z_encode_grad_maps(ptrs, ent.ctypes.data, n, host.ctypes.data)
+    _check("fp8z_encode_grad_maps", rc)
+    return torch.from_numpy(host.copy()).to(device)
+
+
+def fp8z_adamw_requant_step_rowmajor(p, m, v, g_maps, w_row, inv_scale, blk_begin, nblk, hp,
+                                     desc, params, nparams, w_fp8_t=None, inv_scale_t=None,
+                                     dev_status=None, stream=None):
+    """The fused step reading row-major grads (through g_maps) and writing the
+    E4M3 weights row-major into w_row (each param at its t_offset)."""
+    import torch
+    cap = p.numel() // BLOCK_ELEMS
+    for t, name in ((m, "m"), (v, "v")):
+        if t.numel() != p.numel():
+            raise ValueError(f"{name} must have as many elements as p")
+    if inv_scale.numel() < cap:
+        raise ValueError("inv_scale must hold one scale per block")
+    if g_maps.numel() < nparams * 128:
+        raise ValueError("g_maps must hold one 128-byte map per param")
+    rc = lib().fp8z_adamw_requant_step_rowmajor(
+        _dptr(p, torch.float32, "p"), _dptr(m, torch.float32, "m"), _dptr(v, torch.float32, "v"),
+        _dptr(g_maps, torch.uint8, "g_maps"), _dptr(w_row, torch.uint8, "w_row"), w_row.numel(),
+        _dptr(inv_scale, torch.float32, "inv_scale"), cap, int(blk_begin), int(nblk),
+        _dptr(desc, torch.uint8, "desc"), _dptr(params, torch.uint8, "params"), int(nparams),
+        _dptr(w_fp8_t, torch.uint8, "w_fp8_t"), 0 if w_fp8_t is None else w_fp8_t.numel(),
+        _dptr(inv_scale_t, torch.float32, "inv_scale_t"),
+        0 if inv_scale_t is None else inv_scale_t.numel(),
+        ctypes.byref(hp), _dptr(dev_status, torch.int32, "dev_status"), _stream_handle(stream))
+    _check("fp8z_adamw_requant_step_rowmajor", rc)
 
 
 def fp8z_dequant(w_fp8, inv_scale, nblk, out, stream=None):

@@ -187,6 +187,48 @@ FP8Z_API int fp8z_adamw_requant_step(float *p, const float *g, float *m, float *
                             void *stream);
 
 /*
+ * fp8z_adamw_requant_step_rowmajor -- the same step with the layout transform
+ * fused into it (fold-on-read of the grad, unfold-on-write of the FP8
+ * weights).  "A ZeRO Optimizer Design for Blockwise FP8 Quantization",
+ * "Summary": the grad is folded before the update and the gathered FP8 params
+ * are unfolded after it; "Experiments: performance" names that fold/unfold as
+ * the method's extra cost.  Here the kernel reads each block's grad straight
+ * from the param's row-major [e, rows, cols] FP32 grad through a TMA tensor
+ * map (zero past the ragged edge) and writes the block's E4M3 codes straight
+ * into the param's row-major [e, rows, cols] bytes.  p, m, v stay folded (the
+ * optimizer's own state), inv_scale is per folded block (already the
+ * row-major [e, hb, wb] grid of each param).
+ * g_maps: device array of nparams tensor maps (128 bytes each, 64-byte
+ *   aligned) written by fp8z_encode_grad_maps and copied to the device.
+ * w_row / w_row_bytes: device buffer of every param's row-major E4M3 bytes,
+ *   param i at params[i].t_offset (the same offsets as the column-major copy).
+ * desc and params (device) are required.  Other arguments, per-element math,
+ * padding and errors as fp8z_adamw_requant_step; a block whose descriptor
+ * disagrees with the param table gets grad 0, no row-major write, and
+ * FP8Z_EINVAL in *dev_status.
+ */
+FP8Z_API int fp8z_adamw_requant_step_rowmajor(float *p, float *m, float *v, const void *g_maps,
+                                              uint8_t *w_row, int64_t w_row_bytes, float *inv_scale,
+                                              int64_t capacity_blocks, int64_t blk_begin, int64_t nblk,
+                                              const fp8z_block_desc *desc,
+                                              const fp8z_param_entry *params, int32_t nparams,
+                                              uint8_t *w_fp8_t, int64_t w_fp8_t_bytes,
+                                              float *inv_scale_t, int64_t inv_scale_t_count,
+                                              const fp8z_adamw_hparams *hp, int32_t *dev_status,
+                                              void *stream);
+
+/*
+ * fp8z_encode_grad_maps -- host only: the tensor maps the row-major step reads
+ * the grads through.  g_ptrs[i] (host array of device pointers) is param i's
+ * row-major FP32 grad [e, rows, cols]; params[i] its planner entry (host).
+ * Writes nparams maps of 128 bytes to maps_out (host, 64-byte aligned); the
+ * caller copies them to device memory.  Each grad must be 16-byte aligned with
+ * cols a multiple of 4 (FP8Z_EALIGN otherwise).  No device work.
+ */
+FP8Z_API int fp8z_encode_grad_maps(const void *const *g_ptrs, const fp8z_param_entry *params,
+                                   int32_t nparams, void *maps_out);
+
+/*
  * fp8z_dequant -- out[b][i] = E4M3_value(w_fp8[b][i]) * inv_scale[b] (float
  * product), for nblk blocks ("FP8-Flow-MoE" §3.1, D(Q(x)) = Q(x)*s).
  * w_fp8: device u8 [nblk,128,128]; inv_scale: device f32 [nblk];

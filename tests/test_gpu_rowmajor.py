@@ -1,0 +1,116 @@
+"""The fused row-major step (fold-on-read of the grad through TMA tensor maps,
+unfold-on-write of the E4M3 weights) against the oracle: the oracle folds the
+row-major grad, runs its step on the folded state, and unfolds its codes.
+Same bit-exact bar as the folded step."""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+from blockwise_fp8_zero_gb300 import fp8z, workloads  # noqa: E402
+
+from _gpu_util import oracle_blocks  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+BLK = fp8z.BLOCK_ELEMS
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from blockwise_fp8_zero_gb300 import build
+    build.build()
+    fp8z.lib()
+
+
+def run_case(oracle, shapes, dp, split=0, transposed=False, step=5, seed=0, bad_desc=False):
+    params, shards, blocks, summ = fp8z.fp8z_plan_shards(shapes, dp, split)
+    cap = int(summ["capacity_blocks"])
+    dev = torch.device("cuda")
+    state = {}
+    for k, d in zip("pmv", (workloads.Dist("normal", 0.02), workloads.Dist("normal", 2e-4),
+                            workloads.Dist("uniform", 1e-7, 4e-7))):
+        t = torch.empty(cap * BLK)
+        workloads.fill(t, k, d, seed, blocks["valid_rows"], blocks["valid_cols"])
+        state[k] = t
+    gen = torch.Generator().manual_seed(seed + 1)
+    grads = [torch.randn(s, generator=gen) * 1e-3 for s in shapes]
+    # host copies for the oracle, grad folded by the oracle's own fold
+    host = {k: state[k].numpy().copy() for k in "pmv"}
+    g_fold = np.zeros(cap * BLK, np.float32)
+    for i, gt in enumerate(grads):
+        o = int(params[i]["blk_offset"]) * BLK
+        f = oracle.fold(gt.numpy()).ravel()
+        g_fold[o:o + f.size] = f
+    d = {k: state[k].to(dev) for k in "pmv"}
+    gd = [gt.to(dev) for gt in grads]
+    maps = fp8z.fp8z_encode_grad_maps(gd, params)
+    t_bytes = int(sum(e * r * c for e, r, c in shapes))
+    t_scales = int(sum(int(p["e"]) * int(p["hb"]) * int(p["wb"]) for p in params))
+    w_row = torch.zeros(t_bytes, dtype=torch.uint8, device=dev)
+    inv = torch.zeros(cap, device=dev)
+    wt = torch.zeros(t_bytes, dtype=torch.uint8, device=dev) if transposed else None
+    it = torch.zeros(t_scales, device=dev) if transposed else None
+    bl = blocks.copy()
+    if bad_desc:
+        bl["param"][0] = len(shapes) + 3
+    desc = fp8z.table_to_device(bl)
+    pdev = fp8z.table_to_device(params)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    hp = fp8z.hparams(step=step)
+    for s in shards:
+        fp8z.fp8z_adamw_requant_step_rowmajor(d["p"], d["m"], d["v"], maps, w_row, inv,
+                                              int(s["blk_begin"]), int(s["blk_count_real"]), hp,
+                                              desc, pdev, len(params), w_fp8_t=wt, inv_scale_t=it,
+                                              dev_status=st)
+    torch.cuda.synchronize()
+    if bad_desc:
+        return st.item()
+    assert st.item() == 0, fp8z.fp8z_status_string(st.item())
+    wt_o = np.zeros(t_bytes, np.uint8) if transposed else None
+    it_o = np.zeros(t_scales, np.float32) if transposed else None
+    q_o, inv_o = oracle_blocks(oracle, hp, host["p"], g_fold, host["m"], host["v"],
+                               np.ascontiguousarray(blocks).view(oracle.BLOCK_DESC),
+                               np.ascontiguousarray(params).view(oracle.PARAM_ENTRY) if transposed else None,
+                               wt_o, it_o)
+    for k in "pmv":
+        assert np.array_equal(d[k].cpu().numpy().view(np.uint32), host[k].view(np.uint32)), k
+    data = blocks["param"] >= 0
+    assert np.array_equal(inv.cpu().numpy()[data], inv_o[data])
+    want_row = np.zeros(t_bytes, np.uint8)
+    for i, (E, H, W) in enumerate(shapes):
+        pe = params[i]
+        o = int(pe["blk_offset"])
+        nb = E * int(pe["hb"]) * int(pe["wb"])
+        qq = oracle.unfold(q_o[o * BLK:(o + nb) * BLK].astype(np.float32).reshape(nb, 128, 128), E, H, W)
+        t0 = int(pe["t_offset"])
+        want_row[t0:t0 + E * H * W] = qq.astype(np.uint8).ravel()
+    assert np.array_equal(w_row.cpu().numpy(), want_row)
+    if transposed:
+        assert np.array_equal(wt.cpu().numpy(), wt_o)
+        assert np.array_equal(it.cpu().numpy(), it_o)
+
+
+@pytest.mark.parametrize("shapes", [[(1, 256, 384)], [(2, 300, 260)], [(1, 129, 4)], [(3, 7, 1000)],
+                                    [(1, 7168, 576)], [(1, 300, 200), (2, 128, 640), (1, 64, 64)]])
+@pytest.mark.parametrize("transposed", [False, True])
+def test_rowmajor_step(oracle, shapes, transposed):
+    run_case(oracle, shapes, dp=1, transposed=transposed, seed=len(shapes))
+
+
+@pytest.mark.parametrize("split", [0, 1])
+def test_rowmajor_step_sharded(oracle, split):
+    run_case(oracle, [(1, 640, 384), (2, 200, 300), (1, 128, 1000), (1, 1000, 128)], dp=3,
+             split=split, transposed=True, step=9)
+
+
+def test_rowmajor_bad_descriptor_reported(oracle):
+    assert run_case(oracle, [(1, 256, 256)], dp=1, bad_desc=True) == fp8z.FP8Z_EINVAL
+
+
+def test_encode_grad_maps_rejects_unaligned_rows():
+    params, _, _, _ = fp8z.fp8z_plan_shards([(1, 128, 130)], 1, 0, with_blocks=False)
+    g = torch.zeros((1, 128, 130), device="cuda")
+    with pytest.raises(fp8z.Fp8zError):
+        fp8z.fp8z_encode_grad_maps([g], params)
