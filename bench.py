@@ -219,7 +219,7 @@ def run_ours(args):
     build.build()
     fp8z.lib()
 
-    w = workloads.get(args.workload)
+    w = workloads.get(args.workload, args.split)
     if args.max_elems:
         w = workloads.scaled(w, args.max_elems)
     free, total = torch.cuda.mem_get_info(dev)
@@ -340,6 +340,8 @@ def run_ours(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic",
         "config": {"workload": w.name, "params": len(w.shapes), "elements": real, "blocks": nblk_run,
+                   "split": "param-wise" if w.split == 1 else "block-wise",
+                   "padding_bytes_fp32_state": int(summ["fold_pad_elems"] + summ["shard_pad_elems"]) * 16,
                    "dp_shards": w.dp, "column_major_copy": w.transposed, "step": step0,
                    "l2": f"state {cap * BLK * 16 / 1e9:.0f} GB >> 129 MB L2: no flush between steps",
                    "launches_per_step": launches_per_step, "scaled": scaled_note,
@@ -573,6 +575,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="flat6e9")
+    ap.add_argument("--split", type=int, default=None, choices=[0, 1],
+                    help="0 block-wise, 1 param-wise (default: the workload's own)")
     ap.add_argument("--cpu-blocks", type=int, default=24576)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
