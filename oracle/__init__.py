@@ -23,6 +23,7 @@ __all__ = [
     "Hparams", "e4m3_encode", "e4m3_encode_bits_range", "e4m3_decode",
     "adamw_scalars", "adamw_elements", "block_scale", "adamw_requant_step",
     "dequant", "transpose_fp8", "fold", "unfold", "plan_shards", "BLK", "BLK_ELEMS",
+    "quantize_rowwise", "transpose_rowwise", "dequant_rowwise",
 ]
 
 BLK = 128
@@ -93,6 +94,9 @@ def _load():
         lib.fp8z_ref_fold.argtypes = [P, i64, i64, i64, P]
         lib.fp8z_ref_unfold.argtypes = [P, i64, i64, i64, P]
         lib.fp8z_ref_plan_shards.argtypes = [P, i32, i32, i32, P, P, P, i64, P]
+        lib.fp8z_ref_quantize_rowwise.argtypes = [P, i64, i64, ctypes.c_int, P, P]
+        lib.fp8z_ref_transpose_rowwise.argtypes = [P, P, i64, i64, P, P]
+        lib.fp8z_ref_dequant_rowwise.argtypes = [P, P, i64, i64, P]
         lib.fp8z_ref_plan_shards.restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -197,6 +201,36 @@ def unfold(blocks, E, H, W):
     out = np.empty((E, H, W), dtype=np.float32)
     _load().fp8z_ref_unfold(_ptr(blocks), E, H, W, _ptr(out))
     return out
+
+
+def quantize_rowwise(x, pow2=True):
+    """[R, C] float32 (C % 128 == 0) -> (codes [R, C], scales [R, C/128]); 1x128 tiles."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    R, C = x.shape
+    q = np.empty((R, C), np.uint8)
+    s = np.empty((R, C // BLK), np.float32)
+    _load().fp8z_ref_quantize_rowwise(_ptr(x), R, C, int(pow2), _ptr(q), _ptr(s))
+    return q, s
+
+
+def transpose_rowwise(q, s):
+    """Row-wise codes/scales of [R, C] -> column-wise codes [C, R], scales [C, R/128]."""
+    q = np.ascontiguousarray(q, dtype=np.uint8)
+    s = np.ascontiguousarray(s, dtype=np.float32)
+    R, C = q.shape
+    qt = np.empty((C, R), np.uint8)
+    st = np.empty((C, R // BLK), np.float32)
+    _load().fp8z_ref_transpose_rowwise(_ptr(q), _ptr(s), R, C, _ptr(qt), _ptr(st))
+    return qt, st
+
+
+def dequant_rowwise(q, s):
+    q = np.ascontiguousarray(q, dtype=np.uint8)
+    s = np.ascontiguousarray(s, dtype=np.float32)
+    R, C = q.shape
+    x = np.empty((R, C), np.float32)
+    _load().fp8z_ref_dequant_rowwise(_ptr(q), _ptr(s), R, C, _ptr(x))
+    return x
 
 
 def plan_shards(shapes, dp, split, with_blocks=True):

@@ -668,3 +668,90 @@ int fp8z_ref_plan_shards(const ref_param_shape *shapes, int32_t nparams, int32_t
     free(nb);
     return 0;
 }
+
+/* ------------------------------------------------------------------------- */
+/* 1x128-tile row-wise quantization and the scaling-aware transpose.           */
+/* ------------------------------------------------------------------------- */
+/* [FP8-Flow] §3.1: a row-wise quantized tensor has one scale per 128
+ * consecutive elements of a row, s = amax/448 (the dequant multiplier), and
+ * Q(x) = round(x/s) to the nearest E4M3 value.  With power-of-two scales
+ * (s = 2^T) re-expressing a value under another power-of-two scale only moves
+ * its exponent.  READING: pow2 = 1 takes s = 2^ceil(log2(amax/448)), the
+ * smallest power of two that keeps every |x/s| <= 448; a tile of zeros takes
+ * s = 1.  q: [R, C] codes, s: [R, C/128] scales, C a multiple of 128. */
+void fp8z_ref_quantize_rowwise(const float *x, int64_t R, int64_t C, int pow2,
+                               uint8_t *q, float *s)
+{
+    int64_t nt = C / BLK;
+    for (int64_t r = 0; r < R; ++r)
+        for (int64_t t = 0; t < nt; ++t) {
+            const float *xr = x + r * C + t * BLK;
+            float amax = 0.0f;
+            for (int c = 0; c < BLK; ++c)
+                amax = fmaxf(amax, fabsf(xr[c]));
+            double sc;
+            if (amax == 0.0f) {
+                sc = 1.0;
+            } else if (pow2) {
+                /* smallest 2^k >= amax/448, on the exact quotient, kept within
+                 * the normal float range [2^-126, 2^127] */
+                double ratio = (double)amax / 448.0;
+                int e;
+                double f = frexp(ratio, &e);          /* ratio = f * 2^e, f in [0.5,1) */
+                int k = (f == 0.5) ? e - 1 : e;
+                if (k < -126) k = -126;
+                if (k > 127) k = 127;
+                sc = ldexp(1.0, k);
+            } else {
+                sc = (double)(amax / 448.0f);
+            }
+            s[r * nt + t] = (float)sc;
+            for (int c = 0; c < BLK; ++c)
+                q[r * C + t * BLK + c] = fp8z_ref_e4m3_encode((float)((double)xr[c] / (double)(float)sc));
+        }
+}
+
+/* Scaling-aware transpose ([FP8-Flow] §3.1): the column-wise layout of the same
+ * tensor, without going back to high precision.  For the 128x128 tile at
+ * (row tile i, column tile j), every output row c (an input column) takes the
+ * scale s' = max over the tile's 128 input rows of s[r][j] (aligning to the
+ * largest scale avoids overflow), and each code is re-expressed under it:
+ * q'[c][r] = nearest E4M3 value to decode(q[r][c]) * s[r][j] / s'.  With
+ * power-of-two scales this is the page's exponent shift E' = E - D, M' = M
+ * (D = log2 s' - log2 s[r][j]), exact unless the shifted value leaves the
+ * normal range; then it rounds to the nearest subnormal (ties to even).
+ * READING: the re-expression is computed in FP32 -- ratio = s[r][j] / s',
+ * y = decode(q) * ratio, one rounding of y to E4M3 -- every step of which is
+ * exact for power-of-two scales.
+ * q_t: [C, R] codes, s_t: [C, R/128] scales; R and C multiples of 128. */
+void fp8z_ref_transpose_rowwise(const uint8_t *q, const float *s, int64_t R, int64_t C,
+                                uint8_t *q_t, float *s_t)
+{
+    int64_t ntc = C / BLK, ntr = R / BLK;
+    for (int64_t i = 0; i < ntr; ++i)
+        for (int64_t j = 0; j < ntc; ++j) {
+            float smax = 0.0f;
+            for (int r = 0; r < BLK; ++r)
+                smax = fmaxf(smax, s[(i * BLK + r) * ntc + j]);
+            for (int c = 0; c < BLK; ++c) {
+                int64_t oc = j * BLK + c;
+                s_t[oc * ntr + i] = smax;
+                for (int r = 0; r < BLK; ++r) {
+                    int64_t ir = i * BLK + r;
+                    float v = (float)fp8z_ref_e4m3_decode(q[ir * C + oc]);
+                    float ratio = s[ir * ntc + j] / smax;
+                    float y = v * ratio;
+                    q_t[oc * R + ir] = fp8z_ref_e4m3_encode(y);
+                }
+            }
+        }
+}
+
+/* Row-wise dequantize: x[r][c] = decode(q[r][c]) * s[r][c/128] (float). */
+void fp8z_ref_dequant_rowwise(const uint8_t *q, const float *s, int64_t R, int64_t C, float *x)
+{
+    int64_t nt = C / BLK;
+    for (int64_t r = 0; r < R; ++r)
+        for (int64_t c = 0; c < C; ++c)
+            x[r * C + c] = (float)fp8z_ref_e4m3_decode(q[r * C + c]) * s[r * nt + c / BLK];
+}
