@@ -438,6 +438,31 @@ def time_aux_kernels(w, q, inv, params, dev, stream, peak, reps=5, g=None, fused
         qb = torch.empty(E * H * W, dtype=torch.uint8, device=dev)
         timed(lambda: fp8z.fp8z_unfold(q, pe, qb, stream=stream), 2 * E * H * W, "fp8z_unfold_e4m3")
         del qb
+    # 1x128 row-wise quantize + scaling-aware transpose of an activation of
+    # 65536 tokens x 7168 (N(0,1), 0.1 % x60 outliers), power-of-two scales
+    try:
+        T, Hd = 65536, 7168
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(5)
+        xa = torch.randn(T, Hd, generator=gen, device=dev)
+        xa = torch.where(torch.rand(T, Hd, generator=gen, device=dev) < 1e-3, xa * 60, xa)
+        qa = torch.empty(T, Hd, dtype=torch.uint8, device=dev)
+        sa = torch.empty(T, Hd // 128, device=dev)
+        qta = torch.empty(Hd, T, dtype=torch.uint8, device=dev)
+        sta = torch.empty(Hd, T // 128, device=dev)
+    except RuntimeError:
+        return out
+    n = T * Hd
+
+    def timed_act(fn, nbytes, label):
+        timed(fn, nbytes, label)
+        out[label]["param"] = f"{T}x{Hd} activation"
+
+    timed_act(lambda: fp8z.fp8z_quantize_rowwise(xa, True, qa, sa, stream=stream), 5 * n + 4 * n // 128,
+              "fp8z_quantize_rowwise")
+    timed_act(lambda: fp8z.fp8z_transpose_rowwise(qa, sa, qta, sta, stream=stream), 2 * n + 8 * n // 128,
+              "fp8z_transpose_rowwise")
+    del xa, qa, sa, qta, sta
     return out
 
 

@@ -21,7 +21,7 @@ BUILD_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libfp8z.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-CU_SOURCES = ["step.cu", "aux.cu", "fold.cu"]
+CU_SOURCES = ["step.cu", "aux.cu", "fold.cu", "rowwise.cu"]
 CPP_SOURCES = ["host.cpp", "plan.cpp"]
 HEADERS = [os.path.join(CSRC, "fp8z_device.cuh"), os.path.join(CSRC, "fp8z_host.h"),
            os.path.join(INCLUDE, "fp8z.h")]

@@ -45,7 +45,8 @@ assert param_entry_dtype.itemsize == 64 and block_desc_dtype.itemsize == 20
 
 EXPORTED = ("fp8z_plan_shards", "fp8z_adamw_requant_step", "fp8z_adamw_requant_step_rowmajor",
             "fp8z_encode_grad_maps", "fp8z_dequant",
-            "fp8z_transpose_fp8", "fp8z_fold", "fp8z_unfold", "fp8z_e4m3_encode_bits",
+            "fp8z_transpose_fp8", "fp8z_fold", "fp8z_unfold", "fp8z_quantize_rowwise",
+            "fp8z_transpose_rowwise", "fp8z_e4m3_encode_bits",
             "fp8z_watchdog_selftest", "fp8z_status_string")
 
 
@@ -98,6 +99,8 @@ def lib():
         L.fp8z_transpose_fp8.argtypes = [P, P, P, P, P, P]
         L.fp8z_fold.argtypes = [P, i32, P, P, P, P]
         L.fp8z_unfold.argtypes = [P, i32, P, P, P, P]
+        L.fp8z_quantize_rowwise.argtypes = [P, i64, i64, i32, P, P, P]
+        L.fp8z_transpose_rowwise.argtypes = [P, P, i64, i64, P, P, P]
         L.fp8z_e4m3_encode_bits.argtypes = [ctypes.c_uint32, i64, P, P]
         L.fp8z_watchdog_selftest.argtypes = [P, i64, P]
         L.fp8z_status_string.argtypes = [ctypes.c_int]
@@ -308,6 +311,30 @@ def fp8z_unfold(blocks, entry, dst, dev_status=None, stream=None):
                            _dptr(dst, None, "dst"), _dptr(dev_status, torch.int32, "dev_status"),
                            _stream_handle(stream))
     _check("fp8z_unfold", rc)
+
+
+def fp8z_quantize_rowwise(x, pow2, q, s, stream=None):
+    """x: float32 [rows, cols] -> q uint8 [rows, cols], s float32 [rows, cols/128]."""
+    import torch
+    rows, cols = x.shape
+    if q.numel() < rows * cols or s.numel() < rows * (cols // BLOCK):
+        raise ValueError("output buffers too small")
+    rc = lib().fp8z_quantize_rowwise(_dptr(x, torch.float32, "x"), rows, cols, int(bool(pow2)),
+                                     _dptr(q, torch.uint8, "q"), _dptr(s, torch.float32, "s"),
+                                     _stream_handle(stream))
+    _check("fp8z_quantize_rowwise", rc)
+
+
+def fp8z_transpose_rowwise(q, s, q_t, s_t, stream=None):
+    """Row-wise q [rows, cols], s [rows, cols/128] -> column-wise q_t [cols, rows], s_t [cols, rows/128]."""
+    import torch
+    rows, cols = q.shape
+    if q_t.numel() < rows * cols or s_t.numel() < cols * (rows // BLOCK) or s.numel() < rows * (cols // BLOCK):
+        raise ValueError("buffers too small")
+    rc = lib().fp8z_transpose_rowwise(_dptr(q, torch.uint8, "q"), _dptr(s, torch.float32, "s"), rows, cols,
+                                      _dptr(q_t, torch.uint8, "q_t"), _dptr(s_t, torch.float32, "s_t"),
+                                      _stream_handle(stream))
+    _check("fp8z_transpose_rowwise", rc)
 
 
 def fp8z_e4m3_encode_bits(first_bits, n, out, stream=None):

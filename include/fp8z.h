@@ -279,6 +279,33 @@ FP8Z_API int fp8z_unfold(const void *blocks, int32_t elem_bytes, const fp8z_para
                          void *dst, int32_t *dev_status, void *stream);
 
 /*
+ * fp8z_quantize_rowwise -- 1x128-tile row-wise E4M3 quantization ("FP8-Flow-MoE"
+ * §3.1): for each row and each 128 consecutive columns, s = amax/448 (pow2 = 0,
+ * kept >= FLT_MIN) or the smallest power of two >= amax/448 (pow2 = 1, kept in
+ * [2^-126, 2^127]); s = 1 for a tile of zeros; q = E4M3(x/s), nearest even,
+ * saturating.  x: device f32 [rows, cols]; q: device u8 [rows, cols];
+ * s: device f32 [rows, cols/128] (dequant multipliers).  cols % 128 == 0.
+ * Returns FP8Z_OK / EINVAL / EALIGN / EUNSUPPORTED / ECUDA.
+ */
+FP8Z_API int fp8z_quantize_rowwise(const float *x, int64_t rows, int64_t cols, int32_t pow2,
+                                   uint8_t *q, float *s, void *stream);
+
+/*
+ * fp8z_transpose_rowwise -- scaling-aware transpose ("FP8-Flow-MoE" §3.1): the
+ * column-wise (1x128 along columns) layout of a row-wise quantized tensor,
+ * without dequantizing.  For the 128x128 tile at (row tile i, column tile j)
+ * the output scale of each of its 128 output rows is s' = max of the tile's
+ * 128 row scales, and q_t[c][r] = E4M3(decode(q[r][c]) * (s[r][j] / s')),
+ * computed in FP32 -- with power-of-two scales an exact exponent shift except
+ * where the value underflows.  q: device u8 [rows, cols]; s: device f32
+ * [rows, cols/128]; q_t: device u8 [cols, rows]; s_t: device f32
+ * [cols, rows/128].  rows and cols multiples of 128.
+ * Returns FP8Z_OK / EINVAL / EALIGN / EUNSUPPORTED / ECUDA.
+ */
+FP8Z_API int fp8z_transpose_rowwise(const uint8_t *q, const float *s, int64_t rows, int64_t cols,
+                                    uint8_t *q_t, float *s_t, void *stream);
+
+/*
  * fp8z_e4m3_encode_bits -- out[i] = E4M3 code (round to nearest even,
  * saturating, as in the step) of the float whose bit pattern is
  * first_bits + i, for i < n; n a multiple of 4, out device, 16-byte aligned.

@@ -678,7 +678,8 @@ int fp8z_ref_plan_shards(const ref_param_shape *shapes, int32_t nparams, int32_t
  * (s = 2^T) re-expressing a value under another power-of-two scale only moves
  * its exponent.  READING: pow2 = 1 takes s = 2^ceil(log2(amax/448)), the
  * smallest power of two that keeps every |x/s| <= 448; a tile of zeros takes
- * s = 1.  q: [R, C] codes, s: [R, C/128] scales, C a multiple of 128. */
+ * s = 1; scales stay within the normal float range.
+ * q: [R, C] codes, s: [R, C/128] scales, C a multiple of 128. */
 void fp8z_ref_quantize_rowwise(const float *x, int64_t R, int64_t C, int pow2,
                                uint8_t *q, float *s)
 {
@@ -703,7 +704,8 @@ void fp8z_ref_quantize_rowwise(const float *x, int64_t R, int64_t C, int pow2,
                 if (k > 127) k = 127;
                 sc = ldexp(1.0, k);
             } else {
-                sc = (double)(amax / 448.0f);
+                /* amax/448 in float, kept at least the smallest normal float */
+                sc = (double)fmaxf(amax / 448.0f, FLT_MIN);
             }
             s[r * nt + t] = (float)sc;
             for (int c = 0; c < BLK; ++c)
