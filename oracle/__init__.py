@@ -23,7 +23,7 @@ __all__ = [
     "Hparams", "e4m3_encode", "e4m3_encode_bits_range", "e4m3_decode",
     "adamw_scalars", "adamw_elements", "block_scale", "adamw_requant_step",
     "dequant", "transpose_fp8", "fold", "unfold", "plan_shards", "BLK", "BLK_ELEMS",
-    "quantize_rowwise", "transpose_rowwise", "dequant_rowwise",
+    "quantize_rowwise", "transpose_rowwise", "dequant_rowwise", "adamw_requant_step_mx",
 ]
 
 BLK = 128
@@ -94,6 +94,9 @@ def _load():
         lib.fp8z_ref_fold.argtypes = [P, i64, i64, i64, P]
         lib.fp8z_ref_unfold.argtypes = [P, i64, i64, i64, P]
         lib.fp8z_ref_plan_shards.argtypes = [P, i32, i32, i32, P, P, P, i64, P]
+        lib.fp8z_ref_adamw_requant_step_mx.argtypes = [P, P, P, P, P, P, i64, i64, P,
+                                                       ctypes.POINTER(Hparams)]
+        lib.fp8z_ref_adamw_requant_step_mx.restype = ctypes.c_int
         lib.fp8z_ref_quantize_rowwise.argtypes = [P, i64, i64, ctypes.c_int, P, P]
         lib.fp8z_ref_transpose_rowwise.argtypes = [P, P, i64, i64, P, P]
         lib.fp8z_ref_dequant_rowwise.argtypes = [P, P, i64, i64, P]
@@ -166,6 +169,16 @@ def adamw_requant_step(p, g, m, v, w_fp8, inv_scale, blk_begin, nblk, hp,
         ctypes.byref(hp))
     if rc != 0:
         raise ValueError(f"oracle step failed: {rc}")
+
+
+def adamw_requant_step_mx(p, g, m, v, w_fp8, mx_scale, blk_begin, nblk, hp, desc=None):
+    """MXFP8 output variant: in place on p, m, v; writes codes and E8M0 scales
+    ([nblk, 128, 4] bytes, one per 32 elements of a block row)."""
+    rc = _load().fp8z_ref_adamw_requant_step_mx(
+        _ptr(p), _ptr(g), _ptr(m), _ptr(v), _ptr(w_fp8), _ptr(mx_scale), blk_begin, nblk,
+        _ptr(desc), ctypes.byref(hp))
+    if rc != 0:
+        raise ValueError(f"oracle mx step failed: {rc}")
 
 
 def dequant(w_fp8, inv_scale, nblk):

@@ -757,3 +757,70 @@ void fp8z_ref_dequant_rowwise(const uint8_t *q, const float *s, int64_t R, int64
         for (int64_t c = 0; c < C; ++c)
             x[r * C + c] = (float)fp8z_ref_e4m3_decode(q[r * C + c]) * s[r * nt + c / BLK];
 }
+
+/* ------------------------------------------------------------------------- */
+/* MXFP8 output: E4M3 codes with one E8M0 power-of-two scale per 32 elements.  */
+/* ------------------------------------------------------------------------- */
+/* [ZeRO-BFP8] "Blockwise quantization": MXFP8 gives each memory-contiguous
+ * block an E8M0 scale; [FP8-Scale] §3.1: 32-element blocks share an 8-bit
+ * exponent, value = element * 2^(exponent - bias).  READING: the shared
+ * exponent of a group of 32 consecutive elements of a block row is
+ * floor(log2(amax)) - 8 (8 = the largest E4M3 exponent, 448 = 1.75 * 2^8),
+ * clamped to [-127, 127]; E8M0 code = exponent + 127; an all-zero group takes
+ * exponent 0.  Elements are E4M3(x / 2^exponent), nearest even, saturating at
+ * ±448 (the largest element lands in [256, 512)).  Padding (desc) is zero and
+ * enters the amax as zero.
+ * mx_scale: [nblk, 128, 4] bytes (block b at b*512, row r at r*4). */
+int fp8z_ref_adamw_requant_step_mx(float *p, const float *g, float *m, float *v,
+                                   uint8_t *w_fp8, uint8_t *mx_scale,
+                                   int64_t blk_begin, int64_t nblk,
+                                   const ref_block_desc *desc, const ref_hparams *hp)
+{
+    if (nblk < 0 || blk_begin < 0)
+        return -1;
+    float sc[9];
+    fp8z_ref_adamw_scalars(hp, sc);
+    for (int64_t b = blk_begin; b < blk_begin + nblk; ++b) {
+        int64_t base = b * (int64_t)BLK_ELEMS;
+        int vr = BLK, vc = BLK;
+        if (desc) {
+            vr = desc[b].valid_rows;
+            vc = desc[b].valid_cols;
+        }
+        for (int r = 0; r < BLK; ++r) {
+            float row[BLK];
+            for (int c = 0; c < BLK; ++c) {
+                int64_t i = base + r * BLK + c;
+                if (r < vr && c < vc) {
+                    float p1, m1, v1;
+                    fp8z_ref_adamw_element(sc, hp->decay_mode, p[i], g[i], m[i], v[i], &p1, &m1, &v1);
+                    p[i] = p1; m[i] = m1; v[i] = v1;
+                    row[c] = p1;
+                } else {
+                    p[i] = 0.0f; m[i] = 0.0f; v[i] = 0.0f;
+                    row[c] = 0.0f;
+                }
+            }
+            for (int gi = 0; gi < BLK / 32; ++gi) {
+                float amax = 0.0f;
+                for (int c = 0; c < 32; ++c)
+                    amax = fmaxf(amax, fabsf(row[gi * 32 + c]));
+                int ex = 0;
+                if (amax > 0.0f) {
+                    int e2;
+                    (void)frexp((double)amax, &e2);     /* amax = f * 2^e2, f in [0.5,1) */
+                    ex = (e2 - 1) - 8;
+                    if (ex < -127) ex = -127;
+                    if (ex > 127) ex = 127;
+                }
+                mx_scale[b * 512 + r * 4 + gi] = (uint8_t)(ex + 127);
+                for (int c = 0; c < 32; ++c) {
+                    int cc = gi * 32 + c;
+                    float y = (float)((double)row[cc] / ldexp(1.0, ex));
+                    w_fp8[base + r * BLK + cc] = (r < vr && cc < vc) ? fp8z_ref_e4m3_encode(y) : 0;
+                }
+            }
+        }
+    }
+    return 0;
+}

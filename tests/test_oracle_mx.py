@@ -1,0 +1,89 @@
+"""Pins for the oracle's MXFP8 output variant (E8M0 scale per 32 elements of a
+block row; "A ZeRO Optimizer Design for Blockwise FP8 Quantization",
+"Blockwise quantization" on MXFP8, mhpn.cn "Core scaling strategies in FP8
+training" §3.1)."""
+import numpy as np
+
+from _defs import brute_force_encode
+
+BLK = 16384
+
+
+def _state(rng, nblk, spike=True):
+    p = rng.normal(0, 0.02, nblk * BLK).astype(np.float32)
+    g = rng.normal(0, 1e-3, nblk * BLK).astype(np.float32)
+    m = rng.normal(0, 2e-4, nblk * BLK).astype(np.float32)
+    v = (rng.uniform(0.5, 1.5, nblk * BLK) * 4e-7).astype(np.float32)
+    if spike:
+        p[5 * 128 + 40] = 3.0            # block 0, row 5, group 1
+        p[BLK:BLK + 128 * 3] *= 1e-6     # block 1, rows 0-2: tiny values
+        p[2 * BLK:2 * BLK + 64] = 0.0    # block 2, row 0, groups 0-1: zero ...
+        g[2 * BLK:2 * BLK + 64] = 0.0
+        m[2 * BLK:2 * BLK + 64] = 0.0
+        v[2 * BLK:2 * BLK + 64] = 0.0
+    return p, g, m, v
+
+
+def test_mx_step_definition(oracle):
+    rng = np.random.default_rng(0)
+    nblk = 3
+    p, g, m, v = _state(rng, nblk)
+    hp = oracle.Hparams.make(step=4)
+    # the AdamW part is the block-scaled step's
+    pb, gb, mb, vb = (a.copy() for a in (p, g, m, v))
+    oracle.adamw_requant_step(pb, gb, mb, vb, np.zeros(nblk * BLK, np.uint8), np.zeros(nblk, np.float32),
+                              0, nblk, hp)
+    q = np.zeros(nblk * BLK, np.uint8)
+    sc = np.zeros(nblk * 512, np.uint8)
+    oracle.adamw_requant_step_mx(p, g, m, v, q, sc, 0, nblk, hp)
+    assert np.array_equal(p, pb) and np.array_equal(m, mb) and np.array_equal(v, vb)
+    groups = p.reshape(-1, 32)
+    amax = np.max(np.abs(groups), axis=1)
+    X = 2.0 ** (sc.astype(np.float64) - 127)
+    nz = amax > 0
+    ratio = amax[nz] / X[nz]
+    assert np.all((ratio >= 256) & (ratio < 512))          # the largest element lands in [256, 512)
+    assert np.all(sc[~nz] == 127)
+    want = brute_force_encode((groups / X[:, None].astype(np.float64)).astype(np.float32).ravel())
+    assert np.array_equal(q, want)
+    dec = oracle.e4m3_decode(q).reshape(-1, 32) * X[:, None]
+    err = np.abs(dec - groups)
+    sat = np.abs(groups / X[:, None]) > 448
+    # half an E4M3 spacing (<= 16 at the top binade) times the scale, or the saturation gap
+    assert np.all(err[~sat] <= 16 * np.broadcast_to(X[:, None], err.shape)[~sat])
+    assert np.all(err[sat] <= 64 * np.broadcast_to(X[:, None], err.shape)[sat])
+
+
+def test_mx_spike_only_moves_its_group(oracle):
+    rng = np.random.default_rng(1)
+    p, g, m, v = _state(rng, 1, spike=False)
+    hp = oracle.Hparams.make(step=2)
+    q0 = np.zeros(BLK, np.uint8)
+    s0 = np.zeros(512, np.uint8)
+    a = [x.copy() for x in (p, g, m, v)]
+    oracle.adamw_requant_step_mx(*a, q0, s0, 0, 1, hp)
+    p[5 * 128 + 40] = 3.0
+    q1 = np.zeros(BLK, np.uint8)
+    s1 = np.zeros(512, np.uint8)
+    oracle.adamw_requant_step_mx(p, g, m, v, q1, s1, 0, 1, hp)
+    changed = np.nonzero(s0 != s1)[0]
+    assert list(changed) == [5 * 4 + 1]                    # row 5, group 1 only
+
+
+def test_mx_padding_and_desc(oracle):
+    shapes = [(1, 200, 100)]                                # ragged rows and cols
+    params, shards, blocks, summ = oracle.plan_shards(shapes, 1, 0)
+    rng = np.random.default_rng(2)
+    nblk = int(summ["total_blocks"])
+    x = {k: oracle.fold(rng.normal(0, s, (1, 200, 100)).astype(np.float32)).ravel()
+         for k, s in zip("pgm", (0.02, 1e-3, 2e-4))}
+    x["v"] = oracle.fold((rng.uniform(0.5, 1.5, (1, 200, 100)) * 4e-7).astype(np.float32)).ravel()
+    q = np.zeros(nblk * BLK, np.uint8)
+    sc = np.zeros(nblk * 512, np.uint8)
+    oracle.adamw_requant_step_mx(x["p"], x["g"], x["m"], x["v"], q, sc, 0, nblk,
+                                 oracle.Hparams.make(step=3), desc=blocks)
+    blk1 = q[BLK:2 * BLK].reshape(128, 128)                 # block row 1: 72 valid rows
+    assert not np.any(blk1[72:]) and not np.any(blk1[:, 100:])
+    s1 = sc[512:1024].reshape(128, 4)
+    assert np.all(s1[72:] == 127)                           # padding rows: all-zero groups
+    assert np.all(s1[:72, 3] != 127)                        # cols 96..99 of group 3 are real
