@@ -325,6 +325,32 @@ def run_ours(args):
 
     aux = None if (args.no_aux or len(shards) != 1) else time_aux_kernels(
         w, q, inv, params, dev, stream, peak, g=state["g"], fused=fused)
+    if aux is not None:
+        # the MXFP8 output variant of the same step (no column-major copy): codes
+        # + one E8M0 byte per 32 elements, no block-wide amax
+        try:
+            mx = torch.empty(cap * 512, dtype=torch.uint8, device=dev)
+            hp_mx = fp8z.hparams(**{**hp_kw, "step": t})
+            sh = shards[0]
+            ev2 = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+            with torch.cuda.stream(stream):
+                run_mx = lambda: fp8z.fp8z_adamw_requant_step_mx(
+                    state["p"], state["g"], state["m"], state["v"], q, mx, int(sh["blk_begin"]),
+                    int(sh["blk_count_real"]), hp_mx, desc=desc, dev_status=status, stream=stream)
+                run_mx()
+                ev2[0].record(stream)
+                for _ in range(5):
+                    run_mx()
+                ev2[1].record(stream)
+            torch.cuda.synchronize(dev)
+            ms_mx = ev2[0].elapsed_time(ev2[1]) / 5
+            b_mx = nblk_run * (BLK * 29 + 512 + 20)
+            aux["fp8z_adamw_requant_step_mx"] = {"ms": round(ms_mx, 4), "bytes": b_mx,
+                                                 "gbs": round(b_mx / ms_mx / 1e6, 1),
+                                                 "frac": round(b_mx / ms_mx / 1e6 / peak, 4)}
+            del mx
+        except RuntimeError:
+            pass
     if aux and "fp8z_adamw_requant_step_rowmajor" in aux:
         aux["unfused_fold_step_unfold_ms"] = round(
             aux["fp8z_fold_f32"]["ms"] + avg_launch_s * 1e3 + aux["fp8z_unfold_e4m3"]["ms"], 4) \

@@ -103,6 +103,8 @@ struct StepArgs {
     int64_t inv_scale_t_count;
     int32_t* dev_status;
     int64_t timeout_ns;
+    // MXFP8 variant: one E8M0 scale byte per 32 elements of a block row
+    uint8_t* mx_scale;
     // row-major variant: per-param grad tensor maps, whole-param E4M3 buffer
     const CUtensorMap* g_maps;
     uint8_t* w_row;
@@ -167,6 +169,22 @@ __device__ __forceinline__ float block_scale(const StepArgs& A, float amax) {
 }
 
 __device__ __forceinline__ int64_t imin64(int64_t a, int64_t b) { return a < b ? a : b; }
+
+// MXFP8 shared exponent of a group with largest magnitude a: floor(log2 a) - 8
+// (8 = the largest E4M3 exponent, so the largest element lands in [256, 512)),
+// clamped to [-127, 127]; 0 for an all-zero group.
+__device__ __forceinline__ int mx_exponent(float a) {
+    if (a == 0.0f) return 0;
+    const uint32_t b = __float_as_uint(a);
+    const int e = (b >> 23) == 0 ? (31 - __clz(b)) - 149 : int(b >> 23) - 127;
+    const int x = e - 8;
+    return x < -127 ? -127 : (x > 127 ? 127 : x);
+}
+
+// 2^k as a float for k in [-127, 127] (2^-127 is subnormal, still exact).
+__device__ __forceinline__ float exp2i(int k) {
+    return k >= -126 ? __uint_as_float(uint32_t(k + 127) << 23) : __uint_as_float(1u << (k + 149));
+}
 
 __device__ __forceinline__ float4 lds4(const float* p) {
     return *reinterpret_cast<const float4*>(p);
@@ -341,7 +359,7 @@ __device__ __forceinline__ bool column_major_copy(const StepArgs& A, const Block
     return true;
 }
 
-template <bool kRowMajor>
+template <bool kRowMajor, bool kMx>
 __global__ void __launch_bounds__(kThreads, 1) fp8z_step_kernel(const StepArgs A) {
     extern __shared__ __align__(1024) unsigned char smem[];
     float* ring = reinterpret_cast<float*>(smem);
@@ -513,10 +531,27 @@ __global__ void __launch_bounds__(kThreads, 1) fp8z_step_kernel(const StepArgs A
                 store4(A.p + off, p1);
                 store4(A.m + off, m1);
                 store4(A.v + off, v1);
-                keep[kk] = p1;
-                lmax = absmax4(lmax, p1);
+                if constexpr (kMx) {
+                    // MXFP8: the 8 lanes of a 32-element group agree on its
+                    // exponent, then cast right away -- no block-wide amax
+                    float a = absmax4(0.0f, p1);
+                    a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 1));
+                    a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 2));
+                    a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 4));
+                    const int ex = mx_exponent(a);
+                    const float mult = exp2i(-ex);
+                    store_word(A.w_fp8 + off, pack_e4m3x4(__fmul_rn(p1.x, mult), __fmul_rn(p1.y, mult),
+                                                          __fmul_rn(p1.z, mult), __fmul_rn(p1.w, mult)));
+                    if ((lane & 7) == 0)
+                        A.mx_scale[size_t(blk) * (kBlkElems / 32) + size_t(row) * (kBlk / 32) + (lane >> 3)] =
+                            uint8_t(ex + 127);
+                } else {
+                    keep[kk] = p1;
+                    lmax = absmax4(lmax, p1);
+                }
             }
         }
+        if constexpr (kMx) continue;
 
         // ---- block amax: warp shuffle, then one exchange through shared memory
 #pragma unroll
@@ -614,19 +649,19 @@ int prepare(StepArgs& A, float* p, float* m, float* v, float* inv_scale, int64_t
     return FP8Z_OK;
 }
 
-template <bool kRowMajor>
+template <bool kRowMajor, bool kMx = false>
 int launch(const StepArgs& A, void* stream) {
     if (A.nblk == 0) return FP8Z_OK;
     int sms = 0;
     int rc = host::device_sms(&sms);
     if (rc != FP8Z_OK) return rc;
     static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
-    rc = host::set_smem_once(reinterpret_cast<const void*>(&fp8z_step_kernel<kRowMajor>), kRowMajor ? 1 : 0,
-                             int(kSmemBytes));
+    rc = host::set_smem_once(reinterpret_cast<const void*>(&fp8z_step_kernel<kRowMajor, kMx>),
+                             kMx ? 4 : (kRowMajor ? 1 : 0), int(kSmemBytes));
     if (rc != FP8Z_OK) return rc;
     const int64_t grid = A.nblk < sms ? A.nblk : sms;
-    fp8z_step_kernel<kRowMajor><<<dim3(unsigned(grid)), dim3(kThreads), kSmemBytes,
-                                  static_cast<cudaStream_t>(stream)>>>(A);
+    fp8z_step_kernel<kRowMajor, kMx><<<dim3(unsigned(grid)), dim3(kThreads), kSmemBytes,
+                                       static_cast<cudaStream_t>(stream)>>>(A);
     return cudaGetLastError() == cudaSuccess ? FP8Z_OK : FP8Z_ECUDA;
 }
 
@@ -651,7 +686,7 @@ extern "C" int fp8z_adamw_requant_step(float* p, const float* g, float* m, float
     if (rc != FP8Z_OK) return rc;
     A.g = g;
     A.w_fp8 = w_fp8;
-    return launch<false>(A, stream);
+    return launch<false, false>(A, stream);
 }
 
 extern "C" int fp8z_adamw_requant_step_rowmajor(float* p, float* m, float* v, const void* g_maps,
@@ -673,7 +708,27 @@ extern "C" int fp8z_adamw_requant_step_rowmajor(float* p, float* m, float* v, co
     A.g_maps = static_cast<const CUtensorMap*>(g_maps);
     A.w_row = w_row;
     A.w_row_bytes = w_row_bytes;
-    return launch<true>(A, stream);
+    return launch<true, false>(A, stream);
+}
+
+extern "C" int fp8z_adamw_requant_step_mx(float* p, const float* g, float* m, float* v,
+                                          uint8_t* w_fp8, uint8_t* mx_scale, int64_t capacity_blocks,
+                                          int64_t blk_begin, int64_t nblk, const fp8z_block_desc* desc,
+                                          const fp8z_adamw_hparams* hp, int32_t* dev_status,
+                                          void* stream) {
+    if (!g || !w_fp8 || !mx_scale) return FP8Z_EINVAL;
+    if (!host::aligned(g, 16) || !host::aligned(w_fp8, 16)) return FP8Z_EALIGN;
+    // the block inverse-scale buffer is not used; pass the E8M0 buffer to satisfy
+    // the common checks of the state arguments
+    StepArgs A;
+    const int rc = prepare(A, p, m, v, reinterpret_cast<float*>(mx_scale), capacity_blocks, blk_begin,
+                           nblk, desc, nullptr, 0, nullptr, 0, nullptr, 0, hp, dev_status);
+    if (rc != FP8Z_OK) return rc;
+    A.g = g;
+    A.w_fp8 = w_fp8;
+    A.inv_scale = nullptr;
+    A.mx_scale = mx_scale;
+    return launch<false, true>(A, stream);
 }
 
 extern "C" int fp8z_encode_grad_maps(const void* const* g_ptrs, const fp8z_param_entry* params,

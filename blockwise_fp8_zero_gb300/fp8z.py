@@ -44,6 +44,7 @@ plan_summary_dtype = np.dtype([
 assert param_entry_dtype.itemsize == 64 and block_desc_dtype.itemsize == 20
 
 EXPORTED = ("fp8z_plan_shards", "fp8z_adamw_requant_step", "fp8z_adamw_requant_step_rowmajor",
+            "fp8z_adamw_requant_step_mx",
             "fp8z_encode_grad_maps", "fp8z_dequant",
             "fp8z_transpose_fp8", "fp8z_fold", "fp8z_unfold", "fp8z_quantize_rowwise",
             "fp8z_transpose_rowwise", "fp8z_e4m3_encode_bits",
@@ -95,6 +96,8 @@ def lib():
                                                        P, i64, P, i64,
                                                        ctypes.POINTER(fp8z_adamw_hparams), P, P]
         L.fp8z_encode_grad_maps.argtypes = [P, P, i32, P]
+        L.fp8z_adamw_requant_step_mx.argtypes = [P, P, P, P, P, P, i64, i64, i64, P,
+                                                 ctypes.POINTER(fp8z_adamw_hparams), P, P]
         L.fp8z_dequant.argtypes = [P, P, i64, P, P]
         L.fp8z_transpose_fp8.argtypes = [P, P, P, P, P, P]
         L.fp8z_fold.argtypes = [P, i32, P, P, P, P]
@@ -202,6 +205,26 @@ def fp8z_adamw_requant_step(p, g, m, v, w_fp8, inv_scale, blk_begin, nblk, hp,
         0 if inv_scale_t is None else inv_scale_t.numel(),
         ctypes.byref(hp), _dptr(dev_status, torch.int32, "dev_status"), _stream_handle(stream))
     _check("fp8z_adamw_requant_step", rc)
+
+
+def fp8z_adamw_requant_step_mx(p, g, m, v, w_fp8, mx_scale, blk_begin, nblk, hp, desc=None,
+                               dev_status=None, stream=None):
+    """MXFP8 output: E4M3 codes in w_fp8 and one E8M0 byte per 32 elements of a
+    block row in mx_scale (uint8, capacity*512)."""
+    import torch
+    cap = p.numel() // BLOCK_ELEMS
+    for t, name in ((g, "g"), (m, "m"), (v, "v"), (w_fp8, "w_fp8")):
+        if t.numel() != p.numel():
+            raise ValueError(f"{name} must have as many elements as p")
+    if mx_scale.numel() < cap * (BLOCK_ELEMS // 32):
+        raise ValueError("mx_scale must hold 512 bytes per block")
+    rc = lib().fp8z_adamw_requant_step_mx(
+        _dptr(p, torch.float32, "p"), _dptr(g, torch.float32, "g"), _dptr(m, torch.float32, "m"),
+        _dptr(v, torch.float32, "v"), _dptr(w_fp8, torch.uint8, "w_fp8"),
+        _dptr(mx_scale, torch.uint8, "mx_scale"), cap, int(blk_begin), int(nblk),
+        _dptr(desc, torch.uint8, "desc"), ctypes.byref(hp), _dptr(dev_status, torch.int32, "dev_status"),
+        _stream_handle(stream))
+    _check("fp8z_adamw_requant_step_mx", rc)
 
 
 def fp8z_encode_grad_maps(grads, params, device="cuda"):

@@ -218,6 +218,26 @@ FP8Z_API int fp8z_adamw_requant_step_rowmajor(float *p, float *m, float *v, cons
                                               void *stream);
 
 /*
+ * fp8z_adamw_requant_step_mx -- the step with an MXFP8 output instead of the
+ * 128x128 block scales: E4M3 codes with one E8M0 power-of-two scale per 32
+ * consecutive elements of a block row.  "A ZeRO Optimizer Design for Blockwise
+ * FP8 Quantization", "Blockwise quantization" (MXFP8 gives memory-contiguous
+ * blocks an E8M0 scale); mhpn.cn "Core scaling strategies in FP8 training"
+ * §3.1 (32-element blocks share an 8-bit exponent).  Shared exponent
+ * x = floor(log2(amax)) - 8, clamped to [-127, 127] (0 for an all-zero
+ * group); scale byte = x + 127; code = E4M3(p' / 2^x), nearest even,
+ * saturating.  AdamW, padding, p/g/m/v/w_fp8/desc and errors as
+ * fp8z_adamw_requant_step.  mx_scale: device u8 [capacity_blocks, 128, 4]
+ * (block b at b*512, row r at r*4), 4-byte aligned.  Each block needs no
+ * block-wide amax, so there is no per-block synchronisation.
+ */
+FP8Z_API int fp8z_adamw_requant_step_mx(float *p, const float *g, float *m, float *v,
+                                        uint8_t *w_fp8, uint8_t *mx_scale, int64_t capacity_blocks,
+                                        int64_t blk_begin, int64_t nblk, const fp8z_block_desc *desc,
+                                        const fp8z_adamw_hparams *hp, int32_t *dev_status,
+                                        void *stream);
+
+/*
  * fp8z_encode_grad_maps -- host only: the tensor maps the row-major step reads
  * the grads through.  g_ptrs[i] (host array of device pointers) is param i's
  * row-major FP32 grad [e, rows, cols]; params[i] its planner entry (host).

@@ -272,3 +272,35 @@ def test_checkpoint_resume_is_bit_identical(oracle):
     ra, rc = a.results(), c.results()
     for k in ("p", "m", "v", "q", "wt", "it"):
         assert np.array_equal(ra[k], rc[k]), k
+
+
+@pytest.mark.parametrize("shapes", [[(1, 256, 384)], [(2, 130, 257)], [(1, 200, 100), (1, 7, 1000)]])
+def test_mxfp8_step(oracle, shapes):
+    """MXFP8 output variant against the oracle, bit for bit (codes, E8M0 bytes, state)."""
+    c = Case(shapes, dp=2, seed=17)
+    # a spike, tiny values and a zero group
+    x = c.host["p"].reshape(-1, 32)
+    x[3, 5] = 4.0
+    x[10] *= 1e-7
+    for k in "pgmv":
+        c.host[k].reshape(-1, 32)[20] = 0.0
+        c.dev[k].copy_(torch.from_numpy(c.host[k]))
+    hp = fp8z.hparams(step=6)
+    mx = torch.zeros(c.cap * 512, dtype=torch.uint8, device="cuda")
+    for s in c.shards:
+        fp8z.fp8z_adamw_requant_step_mx(c.dev["p"], c.dev["g"], c.dev["m"], c.dev["v"], c.w_fp8, mx,
+                                        int(s["blk_begin"]), int(s["blk_count_real"]), hp,
+                                        desc=c.desc_dev, dev_status=c.status)
+    torch.cuda.synchronize()
+    assert c.status.item() == 0
+    p, g, m, v = (c.host[k].copy() for k in "pgmv")
+    q = np.zeros(c.cap * BLK, np.uint8)
+    sc = np.zeros(c.cap * 512, np.uint8)
+    oracle.adamw_requant_step_mx(p, g, m, v, q, sc, 0, int(c.summary["total_blocks"]),
+                                 oracle.Hparams.make(step=6),
+                                 desc=np.ascontiguousarray(c.blocks).view(oracle.BLOCK_DESC))
+    for k, want in (("p", p), ("m", m), ("v", v)):
+        assert np.array_equal(c.dev[k].cpu().numpy().view(np.uint32), want.view(np.uint32)), k
+    assert np.array_equal(c.w_fp8.cpu().numpy(), q)
+    data = np.repeat(c.blocks["param"] >= 0, 512)
+    assert np.array_equal(mx.cpu().numpy()[data], sc[data])
