@@ -157,12 +157,15 @@ extern "C" int fp8z_dequant(const uint8_t* w_fp8, const float* inv_scale, int64_
     if (!host::aligned(w_fp8, 16) || !host::aligned(out, 16) || !host::aligned(inv_scale, 4))
         return FP8Z_EALIGN;
     if (nblk == 0) return FP8Z_OK;
-    int sms = 0;
-    const int rc = host::device_sms(&sms);
+    int sms = 0, per_sm = 0;
+    int rc = host::device_sms(&sms);
+    if (rc != FP8Z_OK) return rc;
+    rc = host::resident_ctas(reinterpret_cast<const void*>(&dequant_kernel), host::kResidentDequant, 256, 0,
+                             &per_sm);
     if (rc != FP8Z_OK) return rc;
     const int64_t nwords = nblk * (kBlkElems / 4);
     const int64_t want = (nwords + 2047) / 2048;
-    const int64_t cap = int64_t(sms) * 8;
+    const int64_t cap = int64_t(sms) * per_sm;      // one wave: 8 per SM would be 1.3 waves (+3.5 %)
     const unsigned grid = unsigned(want < cap ? want : cap);
     dequant_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(
         reinterpret_cast<const uint32_t*>(w_fp8), inv_scale, nwords, reinterpret_cast<float4*>(out));

@@ -36,6 +36,13 @@ int device_sms(int* sms);
 // cudaFuncSetAttribute(MaxDynamicSharedMemorySize) once per (kernel slot, device).
 int set_smem_once(const void* kernel, int slot, int bytes);
 
+// CTAs of `kernel` that fit on one SM at `threads` threads and `smem` bytes
+// of dynamic shared memory (at least 1), queried once per (kernel slot,
+// device).  Grid-stride kernels launch exactly SMs x this many CTAs: a grid
+// that does not fit in one wave leaves its last CTAs running alone.
+int resident_ctas(const void* kernel, int slot, int threads, int smem, int* per_sm);
+enum ResidentSlot { kResidentQuantizeRowwise = 0, kResidentDequant = 1 };
+
 // The driver's cuTensorMapEncodeTiled (through the runtime's entry-point
 // query, so the library needs no link against libcuda); nullptr if absent.
 void* tensor_map_encoder();

@@ -88,6 +88,25 @@ int set_smem_once(const void* kernel, int slot, int bytes) {
     return FP8Z_OK;
 }
 
+namespace {
+std::atomic<int> g_resident[kMaxSlots][kMaxDevices];
+}  // namespace
+
+int resident_ctas(const void* kernel, int slot, int threads, int smem, int* per_sm) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return FP8Z_ECUDA;
+    const bool cacheable = dev >= 0 && dev < kMaxDevices && slot >= 0 && slot < kMaxSlots;
+    int n = cacheable ? g_resident[slot][dev].load(std::memory_order_acquire) : 0;
+    if (n == 0) {
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, size_t(smem)) != cudaSuccess)
+            return FP8Z_ECUDA;
+        if (n < 1) n = 1;
+        if (cacheable) g_resident[slot][dev].store(n, std::memory_order_release);
+    }
+    *per_sm = n;
+    return FP8Z_OK;
+}
+
 void* tensor_map_encoder() {
     static std::atomic<void*> fn{nullptr};
     void* f = fn.load(std::memory_order_acquire);

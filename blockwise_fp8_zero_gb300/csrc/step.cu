@@ -8,18 +8,26 @@
 // 448/amax with the 1e-6 floor of mhpn.cn "Core scaling strategies in FP8
 // training" §3.2/§4.2; nearest-value E4M3 rounding of "FP8-Flow-MoE" §3.1.
 //
-// Design (GB300): a persistent kernel, one CTA per SM.  One producer warp
+// Design (GB300): a persistent kernel, one CTA per SM.  One producer thread
 // streams each 128x128 block's g, p, m, v through a ring of shared-memory
 // stages with the TMA bulk-copy engine (16 rows x 128 = 2048 floats per
 // tensor per stage), so ~200 KB per SM are in flight independent of register
-// pressure.  Sixteen consumer warps apply AdamW in registers, stream p', m', v'
-// straight back to HBM and keep p' (32 values per thread) until the block's
-// amax is known; the amax comes from warp shuffles plus one shared-memory
-// exchange, then the same registers are cast to E4M3.  HBM traffic is the
-// algorithmic 16 B read + 13 B written per element (+1 B for the optional
-// column-major copy).  The producer keeps loading the next block while the
-// consumers reduce and quantize, so the memory pipe never drains.  Every wait
-// is bounded (fp8z_device.cuh); no tensor cores: the op is element-wise.
+// pressure; it also fetches the next block's descriptor and param entry and
+// hands them over through shared memory.  Sixteen consumer warps apply AdamW
+// in registers, stream p', m', v' straight back to HBM and keep p' (32 values
+// per thread) until the block's amax is known; the amax comes from warp
+// shuffles plus one shared-memory exchange, then the same registers are cast
+// to E4M3.  HBM traffic is the algorithmic 16 B read + 13 B written per
+// element (+1 B for the optional column-major copy).  The producer keeps
+// loading the next block while the consumers reduce and quantize, so the
+// memory pipe never drains.  Every wait is bounded (fp8z_device.cuh); no
+// tensor cores: the op is element-wise.
+//
+// Three instantiations share the pipeline: the block-scaled step on folded
+// buffers; the row-major variant (grad read through TMA tensor maps from each
+// param's [E,H,W] tensor, E4M3 written row-major: the fold/unfold fused in);
+// and the MXFP8 variant (an E8M0 scale per 32 elements, cast stage by stage
+// with no block-wide amax).
 #include <cfloat>
 #include <cmath>
 #include <cstdint>
@@ -39,11 +47,10 @@ namespace {
 // Build-time shape of the pipeline.  The defaults won a sweep on GB300 at
 // 6e9 elements (28.0 ms per step): a deeper ring is faster (4 and 5 stages
 // lose 2-6 %), plain bulk loads beat the L2 evict-first hint (+1.5 %),
-// streaming stores of the FP32 outputs help once the loads are plain.  Losers
-// dropped
-// from the code: L2 prefetch ahead of the ring (-35 %), one contiguous block
-// range per CTA (-2.5 %), streaming stores of the E4M3 bytes (-2.5 %), two
-// rows per warp per stage with 3 stages (-10 %).
+// streaming stores of the FP32 outputs help once the loads are plain.  Dropped
+// from the code after losing: L2 prefetch ahead of the ring (-35 %), one
+// contiguous block range per CTA (-2.5 %), streaming stores of the E4M3 bytes
+// (-2.5 %), two rows per warp per stage with 3 stages (-10 %).
 //   FP8Z_RING             shared-memory stages in the ring
 //   FP8Z_ROWS_PER_WARP    block rows each consumer warp takes per stage
 //   FP8Z_STORE_STREAMING  1: p', m', v' stored with the streaming (.cs) hint
@@ -607,13 +614,14 @@ using namespace fp8z;
 
 namespace {
 
-// Checks shared by both entry points; fills the common fields of A.
-int prepare(StepArgs& A, float* p, float* m, float* v, float* inv_scale, int64_t capacity_blocks,
+// Checks shared by the three step entry points; fills the common fields of A.
+// The per-block output scales (inv_scale or the E8M0 grid) are each entry's own.
+int prepare(StepArgs& A, float* p, float* m, float* v, int64_t capacity_blocks,
             int64_t blk_begin, int64_t nblk, const fp8z_block_desc* desc,
             const fp8z_param_entry* params, int32_t nparams, uint8_t* w_fp8_t,
             int64_t w_fp8_t_bytes, float* inv_scale_t, int64_t inv_scale_t_count,
             const fp8z_adamw_hparams* hp, int32_t* dev_status) {
-    if (!p || !m || !v || !inv_scale || !hp) return FP8Z_EINVAL;
+    if (!p || !m || !v || !hp) return FP8Z_EINVAL;
     if (capacity_blocks < 0 || blk_begin < 0 || nblk < 0) return FP8Z_EINVAL;
     if (capacity_blocks > (INT64_MAX / kBlkElems) / 4) return FP8Z_EINVAL;
     if (blk_begin > capacity_blocks || nblk > capacity_blocks - blk_begin) return FP8Z_ENOSPACE;
@@ -622,13 +630,12 @@ int prepare(StepArgs& A, float* p, float* m, float* v, float* inv_scale, int64_t
                    w_fp8_t_bytes < 0 || inv_scale_t_count < 0))
         return FP8Z_EINVAL;
     if (!host::aligned(p, 16) || !host::aligned(m, 16) || !host::aligned(v, 16) ||
-        !host::aligned(inv_scale, 4) || !host::aligned(desc, 4) || !host::aligned(params, 8) ||
+        !host::aligned(desc, 4) || !host::aligned(params, 8) ||
         !host::aligned(w_fp8_t, 16) || !host::aligned(inv_scale_t, 4) || !host::aligned(dev_status, 4))
         return FP8Z_EALIGN;
     if (!host::hparams_valid(*hp)) return FP8Z_EINVAL;
     std::memset(&A, 0, sizeof(A));
     A.p = p; A.m = m; A.v = v;
-    A.inv_scale = inv_scale;
     A.blk_begin = blk_begin; A.nblk = nblk;
     A.desc = desc;
     A.params = params;
@@ -676,16 +683,18 @@ extern "C" int fp8z_adamw_requant_step(float* p, const float* g, float* m, float
                                        float* inv_scale_t, int64_t inv_scale_t_count,
                                        const fp8z_adamw_hparams* hp, int32_t* dev_status,
                                        void* stream) {
-    if (!g || !w_fp8) return FP8Z_EINVAL;
-    if (!host::aligned(g, 16) || !host::aligned(w_fp8, 16)) return FP8Z_EALIGN;
+    if (!g || !w_fp8 || !inv_scale) return FP8Z_EINVAL;
+    if (!host::aligned(g, 16) || !host::aligned(w_fp8, 16) || !host::aligned(inv_scale, 4))
+        return FP8Z_EALIGN;
     const bool want_t = (w_fp8_t != nullptr) || (inv_scale_t != nullptr);
     StepArgs A;
-    const int rc = prepare(A, p, m, v, inv_scale, capacity_blocks, blk_begin, nblk, desc,
+    const int rc = prepare(A, p, m, v, capacity_blocks, blk_begin, nblk, desc,
                            want_t ? params : nullptr, nparams, w_fp8_t, w_fp8_t_bytes, inv_scale_t,
                            inv_scale_t_count, hp, dev_status);
     if (rc != FP8Z_OK) return rc;
     A.g = g;
     A.w_fp8 = w_fp8;
+    A.inv_scale = inv_scale;
     return launch<false, false>(A, stream);
 }
 
@@ -698,14 +707,17 @@ extern "C" int fp8z_adamw_requant_step_rowmajor(float* p, float* m, float* v, co
                                                 float* inv_scale_t, int64_t inv_scale_t_count,
                                                 const fp8z_adamw_hparams* hp, int32_t* dev_status,
                                                 void* stream) {
-    if (!g_maps || !w_row || !desc || !params || nparams <= 0 || w_row_bytes < 0) return FP8Z_EINVAL;
-    if (!host::aligned(g_maps, 64) || !host::aligned(w_row, 16)) return FP8Z_EALIGN;
+    if (!g_maps || !w_row || !inv_scale || !desc || !params || nparams <= 0 || w_row_bytes < 0)
+        return FP8Z_EINVAL;
+    if (!host::aligned(g_maps, 64) || !host::aligned(w_row, 16) || !host::aligned(inv_scale, 4))
+        return FP8Z_EALIGN;
     StepArgs A;
-    const int rc = prepare(A, p, m, v, inv_scale, capacity_blocks, blk_begin, nblk, desc, params,
+    const int rc = prepare(A, p, m, v, capacity_blocks, blk_begin, nblk, desc, params,
                            nparams, w_fp8_t, w_fp8_t_bytes, inv_scale_t, inv_scale_t_count, hp,
                            dev_status);
     if (rc != FP8Z_OK) return rc;
     A.g_maps = static_cast<const CUtensorMap*>(g_maps);
+    A.inv_scale = inv_scale;
     A.w_row = w_row;
     A.w_row_bytes = w_row_bytes;
     return launch<true, false>(A, stream);
@@ -718,15 +730,12 @@ extern "C" int fp8z_adamw_requant_step_mx(float* p, const float* g, float* m, fl
                                           void* stream) {
     if (!g || !w_fp8 || !mx_scale) return FP8Z_EINVAL;
     if (!host::aligned(g, 16) || !host::aligned(w_fp8, 16)) return FP8Z_EALIGN;
-    // the block inverse-scale buffer is not used; pass the E8M0 buffer to satisfy
-    // the common checks of the state arguments
     StepArgs A;
-    const int rc = prepare(A, p, m, v, reinterpret_cast<float*>(mx_scale), capacity_blocks, blk_begin,
-                           nblk, desc, nullptr, 0, nullptr, 0, nullptr, 0, hp, dev_status);
+    const int rc = prepare(A, p, m, v, capacity_blocks, blk_begin, nblk, desc, nullptr, 0, nullptr, 0,
+                           nullptr, 0, hp, dev_status);
     if (rc != FP8Z_OK) return rc;
     A.g = g;
     A.w_fp8 = w_fp8;
-    A.inv_scale = nullptr;
     A.mx_scale = mx_scale;
     return launch<false, true>(A, stream);
 }
