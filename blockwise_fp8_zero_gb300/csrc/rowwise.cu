@@ -125,6 +125,40 @@ __device__ __forceinline__ uint32_t e4m3x2_scale_f16(uint32_t two_codes, uint32_
     return out;
 }
 
+// The 128 output words of one warp pass set: input columns 4cg..4cg+3
+// (cg = warp + 8h) of rows r0..r0+3, read from the swizzled tile, 4x4
+// byte-transposed, re-expressed and written to output rows 4cg..4cg+3.  The
+// f16x2 / FP32 choice is made once per tile, outside these loops.
+template <bool kF16>
+__device__ __forceinline__ void transpose_tile_words(const uint32_t* tile, int warp, int r0, uint8_t* out,
+                                                     int64_t R, uint32_t rr01, uint32_t rr23,
+                                                     const float (&ratio)[4]) {
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+        const int cg = warp + 8 * h;                     // input columns 4cg..4cg+3
+        uint32_t w4[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) w4[k] = tile[(r0 + k) * 32 + (cg ^ tile_swz(r0 + k))];
+        uint32_t o[4];
+        transpose4x4(w4[0], w4[1], w4[2], w4[3], o[0], o[1], o[2], o[3]);
+        uint8_t* dst = out + int64_t(4 * cg) * R;
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+            uint32_t word = o[cc];                       // bytes: rows r0..r0+3 of column 4cg+cc
+            if (kF16) {
+                word = e4m3x2_scale_f16(word, rr01) | (e4m3x2_scale_f16(word >> 16, rr23) << 16);
+            } else {
+                const float2 a = e4m3x2_to_float2(word);
+                const float2 b = e4m3x2_to_float2(word >> 16);
+                word = pack_e4m3x4(__fmul_rn(a.x, ratio[0]), __fmul_rn(a.y, ratio[1]),
+                                   __fmul_rn(b.x, ratio[2]), __fmul_rn(b.y, ratio[3]));
+            }
+            *reinterpret_cast<uint32_t*>(dst) = word;
+            dst += R;
+        }
+    }
+}
+
 // Re-express one staged 128x128 tile (row tile i, column tile j) under its
 // largest row scale and write it column-wise.  Lane l of every warp owns input
 // rows 4l..4l+3: it reads their four row scales, the warp reduces the tile's
@@ -160,48 +194,34 @@ __device__ __forceinline__ void transpose_tile_out(const uint32_t* tile, const f
     const uint32_t rr01 = f16x2_pack(ratio[0], ratio[1]);
     const uint32_t rr23 = f16x2_pack(ratio[2], ratio[3]);
     if (write_st) st[(j * kTile + st_row) * ntr + i] = smax;
-
-#pragma unroll
-    for (int h = 0; h < 4; ++h) {
-        const int cg = warp + 8 * h;                     // input columns 4cg..4cg+3
-        uint32_t w4[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) w4[k] = tile[(r0 + k) * 32 + (cg ^ tile_swz(r0 + k))];
-        uint32_t o[4];
-        transpose4x4(w4[0], w4[1], w4[2], w4[3], o[0], o[1], o[2], o[3]);
-#pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
-            uint32_t word = o[cc];                       // bytes: rows r0..r0+3 of column 4cg+cc
-            if (warp_f16) {
-                word = e4m3x2_scale_f16(word, rr01) | (e4m3x2_scale_f16(word >> 16, rr23) << 16);
-            } else {
-                const float2 a = e4m3x2_to_float2(word);
-                const float2 b = e4m3x2_to_float2(word >> 16);
-                word = pack_e4m3x4(__fmul_rn(a.x, ratio[0]), __fmul_rn(a.y, ratio[1]),
-                                   __fmul_rn(b.x, ratio[2]), __fmul_rn(b.y, ratio[3]));
-            }
-            const int64_t c = j * kTile + 4 * cg + cc;
-            *reinterpret_cast<uint32_t*>(qt + c * R + i * kTile + r0) = word;
-        }
-    }
+    uint8_t* out = qt + (j * kTile) * R + i * kTile + r0;
+    if (warp_f16)
+        transpose_tile_words<true>(tile, warp, r0, out, R, rr01, rr23, ratio);
+    else
+        transpose_tile_words<false>(tile, warp, r0, out, R, rr01, rr23, ratio);
 }
 
 // One CTA per strip of kW column tiles of one row tile: the strip's rows are
 // read as kW*128 contiguous bytes, staged in swizzled shared tiles with their
 // row scales, then each tile is written out column-wise by all eight warps.
 // Consecutive CTAs take consecutive row tiles of one strip, so their output
-// rows continue each other in memory.  Measured on GB300 at 65536x7168: 0.174 ms
-// with two-tile strips, 0.189 ms with one tile per CTA (128-byte reads per row),
-// 0.201 ms with column tiles fastest; a persistent variant that moved the tiles
-// with TMA (128B-swizzled loads and stores) reached 0.181 ms: the re-expression
-// arithmetic, not the memory system, sets the pace.
+// rows continue each other in memory.  Measured on GB300 at 65536x7168: 0.172
+// ms with two-tile strips, 0.189 ms with one tile per CTA (128-byte reads per
+// row), 0.201 ms with column tiles fastest; a persistent variant that moved the
+// tiles with TMA (128B-swizzled loads and stores) reached 0.181 ms: the
+// re-expression arithmetic, not the memory system, sets the pace.  The tile
+// loop stays rolled: unrolled, the two copies of both re-expression paths
+// ran at 0.218 ms.  Tiles are kTileWords apart, not 4096, so the two tiles'
+// row writes fall on different banks.
+constexpr int kTileWords = kTile * kTile / 4 + 2;
+
 template <int kW>
 __global__ void __launch_bounds__(256) transpose_rowwise_kernel(const uint8_t* __restrict__ q,
                                                                 const float* __restrict__ s,
                                                                 int64_t R, int64_t C,
                                                                 uint8_t* __restrict__ qt,
                                                                 float* __restrict__ st) {
-    __shared__ uint32_t tile[kW][kTile * kTile / 4];
+    __shared__ uint32_t tile[kW][kTileWords];
     __shared__ float scales[kW][kTile];
     const int64_t ntc = C / kTile, ntr = R / kTile;
     const int64_t i = blockIdx.x % ntr, jw = (blockIdx.x / ntr) * kW;   // first column tile of the strip
@@ -231,7 +251,7 @@ __global__ void __launch_bounds__(256) transpose_rowwise_kernel(const uint8_t* _
         row[(w0 + 3) ^ sw] = buf[it].w;
     }
     __syncthreads();
-#pragma unroll
+#pragma unroll 1
     for (int u = 0; u < kW; ++u)
         transpose_tile_out(tile[u], scales[u], i, jw + u, R, ntr, qt, st, warp, lane, tid < kTile, tid);
 }
