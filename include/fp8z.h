@@ -228,8 +228,9 @@ FP8Z_API int fp8z_adamw_requant_step_rowmajor(float *p, float *m, float *v, cons
  * group); scale byte = x + 127; code = E4M3(p' / 2^x), nearest even,
  * saturating.  AdamW, padding, p/g/m/v/w_fp8/desc and errors as
  * fp8z_adamw_requant_step.  mx_scale: device u8 [capacity_blocks, 128, 4]
- * (block b at b*512, row r at r*4), 4-byte aligned.  Each block needs no
- * block-wide amax, so there is no per-block synchronisation.
+ * (block b at b*512, row r at r*4), written byte by byte (no alignment
+ * needed; nullptr is FP8Z_EINVAL).  Each block needs no block-wide amax, so
+ * there is no per-block synchronisation.
  */
 FP8Z_API int fp8z_adamw_requant_step_mx(float *p, const float *g, float *m, float *v,
                                         uint8_t *w_fp8, uint8_t *mx_scale, int64_t capacity_blocks,

@@ -150,3 +150,33 @@ def test_aux_argument_errors(L):
     assert L.fp8z_watchdog_selftest(A16, -1, None) == fp8z.FP8Z_EINVAL
     assert L.fp8z_watchdog_selftest(A16, 10 ** 11, None) == fp8z.FP8Z_EINVAL
     assert L.fp8z_watchdog_selftest(None, 1000, None) == fp8z.FP8Z_EINVAL
+
+
+def test_rowwise_and_mx_argument_errors(L):
+    # 1x128 row-wise quantize / transpose: zero rows is an empty call, a row
+    # length that is not a multiple of 128 or a bad pow2 flag is refused
+    assert L.fp8z_quantize_rowwise(A16, 0, 256, 1, A16, A16, None) == fp8z.FP8Z_OK
+    assert L.fp8z_quantize_rowwise(A16, 4, 0, 1, A16, A16, None) == fp8z.FP8Z_OK
+    assert L.fp8z_quantize_rowwise(A16, 4, 100, 1, A16, A16, None) == fp8z.FP8Z_EINVAL
+    assert L.fp8z_quantize_rowwise(A16, 4, 128, 2, A16, A16, None) == fp8z.FP8Z_EINVAL
+    assert L.fp8z_quantize_rowwise(A16, -1, 128, 1, A16, A16, None) == fp8z.FP8Z_EINVAL
+    assert L.fp8z_quantize_rowwise(A4, 4, 128, 1, A16, A16, None) == fp8z.FP8Z_EALIGN
+    assert L.fp8z_quantize_rowwise(None, 4, 128, 1, A16, A16, None) == fp8z.FP8Z_EINVAL
+    assert L.fp8z_transpose_rowwise(A16, A16, 0, 128, A16, A16, None) == fp8z.FP8Z_OK
+    assert L.fp8z_transpose_rowwise(A16, A16, 100, 128, A16, A16, None) == fp8z.FP8Z_EINVAL
+    assert L.fp8z_transpose_rowwise(A16, A16, 128, 130, A16, A16, None) == fp8z.FP8Z_EINVAL
+    assert L.fp8z_transpose_rowwise(A4, A16, 128, 128, A16, A16, None) == fp8z.FP8Z_EALIGN
+    # MXFP8 step: same state checks as the block-scaled step, its own scale output
+    hp = fp8z.hparams()
+    mx = lambda **k: L.fp8z_adamw_requant_step_mx(
+        k.get("p", A16), A16, A16, A16, k.get("q", A16), k.get("s", A16), 4, k.get("b0", 0),
+        k.get("nb", 0), None, ctypes.byref(k.get("hp", hp)), None, None)
+    assert mx() == fp8z.FP8Z_OK                                  # nblk == 0: nothing launched
+    assert mx(s=A16 + 1) == fp8z.FP8Z_OK                         # E8M0 bytes need no alignment
+    assert mx(s=None) == fp8z.FP8Z_EINVAL
+    assert mx(p=None) == fp8z.FP8Z_EINVAL
+    assert mx(q=A4) == fp8z.FP8Z_EALIGN
+    assert mx(b0=3, nb=2) == fp8z.FP8Z_ENOSPACE
+    bad = fp8z.hparams()
+    bad.eps = 0.0
+    assert mx(hp=bad) == fp8z.FP8Z_EINVAL
