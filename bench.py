@@ -394,10 +394,13 @@ def run_ours(args):
 
 def time_aux_kernels(w, q, inv, params, dev, stream, peak, reps=5, g=None, fused=None):
     """Dequantize, the standalone column-major transpose, unfold/fold of the
-    FP32 grad and unfold of the E4M3 codes, each timed with CUDA events against
-    its algorithmic bytes (dequant: 1 B read + 4 B written per element + 4 B per
-    block; transpose: 1 + 1 B per element + 8 B per block; FP32 fold/unfold:
-    4 + 4 B per element; byte unfold: 1 + 1 B per element)."""
+    FP32 grad, the fused row-major step, unfold of the E4M3 codes, and the 1x128
+    row-wise quantize + scaling-aware transpose of a 65536x7168 activation, each
+    timed with CUDA events against its algorithmic bytes (dequant: 1 B read + 4 B
+    written per element + 4 B per block; transpose: 1 + 1 B per element + 8 B per
+    block; FP32 fold/unfold: 4 + 4 B per element; byte unfold: 1 + 1 B per
+    element; row-wise quantize: 4 + 1 B per element + 4 B per 128; row-wise
+    transpose: 1 + 1 B per element + 8 B per 128)."""
     import torch
     from blockwise_fp8_zero_gb300 import fp8z
     out = {}
