@@ -39,6 +39,17 @@
  *                          §3.1); power-of-two layout change is exact.
  *   fold / unfold       -- torch view/permute of [ZeRO-BFP8] "Layout transform".
  *   planner             -- hand-computed tables and invariants.
+ *   row-wise 1x128      -- quantizer: brute-force nearest encode of x/s per tile,
+ *                          s the smallest power of two >= amax/448 (or amax/448);
+ *                          transpose: with power-of-two scales every code moves
+ *                          by E' = E - D, M' = M except where it underflows, and
+ *                          the double-quantization error of dequantize ->
+ *                          transpose -> requantize ([FP8-Flow] §3.1).
+ *   MXFP8 step          -- AdamW values equal the block-scaled step's; every
+ *                          group's largest element lands in [256, 512) times its
+ *                          E8M0 scale; codes equal a brute-force nearest encode
+ *                          of p'/2^x; a spike moves only its own group's scale;
+ *                          padding and descriptors as in the block-scaled step.
  */
 #include <math.h>
 #include <stdint.h>
