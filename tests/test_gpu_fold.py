@@ -24,6 +24,9 @@ def _lib():
 
 SHAPES = [(1, 256, 384), (2, 300, 260), (1, 129, 1), (3, 7, 1000), (1, 130, 257), (1, 7168, 576),
           (2, 1, 4096)]
+# extreme aspect ratios: a 2 MB row pitch (4096 blocks per block row), 4097
+# block rows, and 4096 one-block experts (the tensor maps' outer dimension)
+EXTREME = [(1, 130, 1 << 19), (1, (1 << 19) + 5, 136), (4096, 16, 16)]
 
 
 def _entry(shape):
@@ -31,7 +34,7 @@ def _entry(shape):
     return params[0]
 
 
-@pytest.mark.parametrize("shape", SHAPES)
+@pytest.mark.parametrize("shape", SHAPES + EXTREME)
 def test_fold_unfold_fp32(oracle, shape):
     E, H, W = shape
     x = torch.randn(shape, generator=torch.Generator().manual_seed(E * H + W))
@@ -49,7 +52,7 @@ def test_fold_unfold_fp32(oracle, shape):
     assert np.array_equal(back.cpu().numpy(), oracle.unfold(want.reshape(-1, 128, 128), E, H, W))
 
 
-@pytest.mark.parametrize("shape", SHAPES)
+@pytest.mark.parametrize("shape", SHAPES + EXTREME)
 def test_fold_unfold_bytes(oracle, shape):
     E, H, W = shape
     g = torch.Generator().manual_seed(W)

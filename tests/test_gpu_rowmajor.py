@@ -99,6 +99,12 @@ def test_rowmajor_step(oracle, shapes, transposed):
     run_case(oracle, shapes, dp=1, transposed=transposed, seed=len(shapes))
 
 
+@pytest.mark.parametrize("shapes", [[(1, 130, 65536)], [(1, 65541, 136)], [(512, 16, 16)]])
+def test_rowmajor_step_extreme_shapes(oracle, shapes):
+    # a 256 KB grad row pitch, 513 block rows, 512 one-block experts
+    run_case(oracle, shapes, dp=1, transposed=True, seed=11)
+
+
 @pytest.mark.parametrize("split", [0, 1])
 def test_rowmajor_step_sharded(oracle, split):
     run_case(oracle, [(1, 640, 384), (2, 200, 300), (1, 128, 1000), (1, 1000, 128)], dp=3,
