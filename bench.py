@@ -356,6 +356,42 @@ def run_ours(args):
             aux["fp8z_fold_f32"]["ms"] + avg_launch_s * 1e3 + aux["fp8z_unfold_e4m3"]["ms"], 4) \
             if "fp8z_unfold_e4m3" in aux else None
 
+    # ---- several shards: the same step as one launch over every block (shard
+    # padding included, masked by the descriptors) and the rank-0 shard alone
+    shard_timing = None
+    if len(shards) > 1:
+        def timed_ranges(ranges, reps=5):
+            hp_s = fp8z.hparams(**{**hp_kw, "step": t})
+            evs = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+
+            def go():
+                for b0, nb in ranges:
+                    fp8z.fp8z_adamw_requant_step(
+                        state["p"], state["g"], state["m"], state["v"], q, inv, b0, nb, hp_s, desc=desc,
+                        params=pdev if w.transposed else None, nparams=len(params) if w.transposed else 0,
+                        w_fp8_t=wt, inv_scale_t=it, dev_status=status, stream=stream)
+            with torch.cuda.stream(stream):
+                go()
+                evs[0].record(stream)
+                for _ in range(reps):
+                    go()
+                evs[1].record(stream)
+            torch.cuda.synchronize(dev)
+            return evs[0].elapsed_time(evs[1]) / reps
+        one_ms = timed_ranges([(0, cap)])
+        a0, n0 = int(shards[0]["blk_begin"]), int(shards[0]["blk_count_real"])
+        r0_ms = timed_ranges([(a0, n0)])
+        r0_real = int(np.sum(blocks["valid_rows"][a0:a0 + n0].astype(np.int64)
+                             * blocks["valid_cols"][a0:a0 + n0].astype(np.int64)))
+        if status.item() != 0:
+            raise RuntimeError(fp8z.fp8z_status_string(status.item()))
+        shard_timing = {
+            "per_shard_launches_ms": round(total_ms / args.steps, 4),
+            "all_shards_one_launch_ms": round(one_ms, 4),
+            "all_shards_one_launch_gelem_s": round(real / (one_ms / 1e3) / 1e9, 4),
+            "rank0_shard_ms": round(r0_ms, 4), "rank0_blocks": n0,
+            "rank0_gelem_s": round(r0_real / (r0_ms / 1e3) / 1e9, 4)}
+
     # ---- end to end through the C ABI with pinned host buffers
     e2e = None if args.no_e2e else run_e2e(args, w, state, q, inv, wt, it, desc, pdev, params,
                                             shards, hp_kw, t, dev, ws)
@@ -379,6 +415,7 @@ def run_ours(args):
                      "peak_source": peak_src,
                      "kernel": "fp8z_step_kernel", "kernel_ms": round(avg_launch_s * 1e3, 4)},
         "aux_kernels": aux,
+        "shard_timing": shard_timing,
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
         "e2e": e2e,
