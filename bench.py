@@ -572,6 +572,31 @@ def run_e2e(args, w, state, q, inv, wt, it, desc, pdev, params, shards, hp_kw, t
     h2d = e_blocks * BLK * 4
     d2h = e_blocks * BLK + e_blocks * 4 + ((e_blocks * BLK + e_blocks * 4) if w.transposed else 0)
 
+    # the host link as it is on this machine right now: pinned copies of up to 2 GB
+    # each way (the device grad gets back its own host copy; the host code
+    # buffer is overwritten by the timed steps anyway)
+    nb_in = min(g_host.numel(), (2 << 30) // 4)
+    nb_out = min(q_host.numel(), 2 << 30)
+
+    def link(fn_in, fn_out):
+        torch.cuda.synchronize(dev)
+        t_ = time.perf_counter()
+        if fn_in:
+            with torch.cuda.stream(s_in):
+                fn_in()
+        if fn_out:
+            with torch.cuda.stream(s_out):
+                fn_out()
+        torch.cuda.synchronize(dev)
+        return time.perf_counter() - t_
+    cp_in = lambda: state["g"][:nb_in].copy_(g_host[:nb_in], non_blocking=True)
+    cp_out = lambda: q_host[:nb_out].copy_(q[:nb_out], non_blocking=True)
+    link(cp_in, cp_out)
+    t_in, t_out, t_both = link(cp_in, None), link(None, cp_out), link(cp_in, cp_out)
+    h2d_gbs, d2h_gbs = nb_in * 4 / t_in / 1e9, nb_out / t_out / 1e9
+    both_gbs = (nb_in * 4 + nb_out) / t_both / 1e9
+    bound_s = max(h2d / (h2d_gbs * 1e9), d2h / (d2h_gbs * 1e9), (h2d + d2h) / (both_gbs * 1e9))
+
     ran = [None] * len(units)      # kernel done with unit u (its g may be overwritten)
     sent = [None] * len(units)     # outputs of unit u copied out (they may be overwritten)
 
@@ -613,6 +638,11 @@ def run_e2e(args, w, state, q, inv, wt, it, desc, pdev, params, shards, hp_kw, t
     real = sum(u[3] for u in units)
     return {"value": round(real * steps * ws / secs / 1e9, 4), "unit": UNIT,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
+            "link": {"h2d_gbs": round(h2d_gbs, 1), "d2h_gbs": round(d2h_gbs, 1),
+                     "both_gbs": round(both_gbs, 1),
+                     "bound_gelem_s": round(real * ws / bound_s / 1e9, 2),
+                     "note": "pinned copies measured just before the timed steps; the bound is "
+                             "max(in / h2d, out / d2h, (in + out) / both)"},
             "units": f"{len(units)} of {nunits} tiles" if len(units) < nunits else f"all {nunits} tiles",
             "note": "grads in, E4M3 weights + scales out per step; FP32 state resident"}
 
