@@ -1,7 +1,10 @@
 // aux.cu -- dequantize, standalone column-major transpose, the E4M3 cast on
 // its own, and the watchdog self-test (sm_103a).
 #include <cstdint>
+#include <cstring>
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include "fp8z.h"
@@ -113,6 +116,105 @@ __global__ void __launch_bounds__(256) transpose_kernel(const TransposeArgs T) {
     }
 }
 
+// The same copy moved by the TMA engine (row length a multiple of 16 bytes).
+// Persistent CTAs, two per SM: one thread loads each folded block with a
+// 128B-swizzled tensor-map load into a ring of kTStages tiles, the eight warps
+// transpose it into one of kTOut swizzled output tiles, and the thread writes
+// that tile with a 3-D tensor-map store that clips at the param's edges (rows
+// and cols of each expert).  Lane l takes the 4x4-byte pieces of input rows
+// 4g..4g+3 with g = ((l & 15) << 1) | (l >> 4) and input column words
+// (l & 15) ^ u for the warp's four units u: with the 128B swizzle on both tiles
+// every shared load and store of a warp touches 32 distinct banks.  Measured on
+// GB300 (32 tiles of 7168^2): 0.97-0.99 of the copy bandwidth against 0.90 for
+// the one-CTA-per-block kernel above, whose global loads, shared round trip and
+// stores run back to back in each CTA.
+constexpr int kTStages = 4, kTOut = 2;
+constexpr int kTileBytesT = kBlkElems;
+constexpr int kTSmemBytes = (kTStages + kTOut) * kTileBytesT + 1024;
+
+struct TransposeTmaArgs {
+    const float* inv;          // the param's first scale
+    float* inv_t;              // [E, Wb, Hb]
+    int64_t nb, hb, wb;
+    int32_t* dev_status;
+    int64_t timeout_ns;
+};
+
+__global__ void __launch_bounds__(256) transpose_tma_kernel(const __grid_constant__ CUtensorMap in_map,
+                                                            const __grid_constant__ CUtensorMap out_map,
+                                                            const TransposeTmaArgs T) {
+    extern __shared__ __align__(1024) unsigned char smem[];
+    unsigned char* in0 = smem;
+    unsigned char* out0 = smem + kTStages * kTileBytesT;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (kTStages + kTOut) * kTileBytesT);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + kTStages);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const uint32_t bar0 = smem_addr(bars);
+    if (smem_addr(smem) & 1023) {          // the swizzle pattern assumes 1024-byte aligned tiles
+        if (tid == 0) report_status(T.dev_status, FP8Z_EALIGN);
+        return;
+    }
+    if (tid == 0) {
+        for (int q = 0; q < kTStages; ++q) mbar_init(bar0 + 8 * q, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    const Watchdog wd{abort_flag, T.dev_status, T.timeout_ns};
+    const int64_t count = (T.nb - blockIdx.x + gridDim.x - 1) / gridDim.x;   // grid <= nb
+    auto issue = [&](int64_t k) {
+        const int64_t b = blockIdx.x + k * gridDim.x;
+        const int q = int(k % kTStages);
+        mbar_arrive_expect_tx(bar0 + 8 * q, kTileBytesT);
+        tma_load_2d(smem_addr(in0 + q * kTileBytesT), &in_map, 0, int(b * kBlk), bar0 + 8 * q);
+    };
+    if (tid == 0)
+        for (int64_t k = 0; k < count && k < kTStages; ++k) issue(k);
+    const int g = ((lane & 15) << 1) | (lane >> 4);       // this lane's input rows 4g..4g+3
+    const int64_t per = T.hb * T.wb;
+    int64_t k = 0;
+    for (; k < count; ++k) {
+        const int64_t b = blockIdx.x + k * gridDim.x;
+        const int64_t e = b / per, brow = (b % per) / T.wb, bcol = b % T.wb;
+        const int q = int(k % kTStages), ob = int(k % kTOut);
+        if (tid == 0) {
+            bulk_wait_read<kTOut - 1>();                   // output tile ob is free again
+            T.inv_t[e * per + bcol * T.hb + brow] = T.inv[b];
+        }
+        mbar_wait_bounded(bar0 + 8 * q, uint32_t((k / kTStages) & 1), wd);
+        __syncthreads();
+        if (*abort_flag) break;
+        const unsigned char* tin = in0 + q * kTileBytesT;
+        unsigned char* tout = out0 + ob * kTileBytesT;
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+            const int cg = (lane & 15) ^ (warp * 4 + h);  // input columns 4cg..4cg+3
+            uint32_t w4[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                w4[i] = *reinterpret_cast<const uint32_t*>(tin + swz128(4 * g + i, 4 * cg));
+            uint32_t o[4];
+            transpose4x4(w4[0], w4[1], w4[2], w4[3], o[0], o[1], o[2], o[3]);
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc)                // output row 4cg+cc, bytes 4g..4g+3
+                *reinterpret_cast<uint32_t*>(tout + swz128(4 * cg + cc, 4 * g)) = o[cc];
+        }
+        fence_proxy_async();
+        __syncthreads();
+        if (tid == 0) {
+            tma_store_3d(&out_map, int(brow * kBlk), int(bcol * kBlk), int(e), smem_addr(tout));
+            bulk_commit();
+            if (k + kTStages < count) issue(k + kTStages);
+        }
+    }
+    if (tid == 0) {
+        if (k < count)                                     // gave up: let the issued loads land
+            for (int64_t kk = k; kk < count && kk < k + kTStages; ++kk)
+                mbar_wait_bounded(bar0 + 8 * int(kk % kTStages), uint32_t((kk / kTStages) & 1), wd, false);
+        bulk_wait_all();
+    }
+}
+
 // ---------------------------------------------------- E4M3 cast on its own
 __global__ void encode_bits_kernel(uint32_t first, int64_t nwords, uint32_t* out) {
     const int64_t stride = int64_t(gridDim.x) * blockDim.x;
@@ -172,9 +274,38 @@ extern "C" int fp8z_dequant(const uint8_t* w_fp8, const float* inv_scale, int64_
     return cudaGetLastError() == cudaSuccess ? FP8Z_OK : FP8Z_ECUDA;
 }
 
+namespace {
+
+// The tensor maps of the TMA transpose: the param's folded blocks as a 2-D
+// byte matrix of 128-byte rows, and the column-major output as [E, W, H]
+// bytes.  False when a dimension is out of the engine's range.
+bool transpose_maps(const fp8z_param_entry& pe, const uint8_t* blocks, uint8_t* out, CUtensorMap* in_map,
+                    CUtensorMap* out_map) {
+    auto enc = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(host::tensor_map_encoder());
+    const int64_t nb = pe.e * pe.hb * pe.wb;
+    if (!enc || nb * kBlk > 0x7FFFFFFFLL || pe.rows > 0x7FFFFFFFLL || pe.cols > 0x7FFFFFFFLL ||
+        pe.e > 0x7FFFFFFFLL)
+        return false;
+    const cuuint32_t box2[2] = {kBlk, kBlk}, box3[3] = {kBlk, kBlk, 1}, one[3] = {1, 1, 1};
+    const cuuint64_t in_dims[2] = {cuuint64_t(kBlk), cuuint64_t(nb * kBlk)};
+    const cuuint64_t in_strides[1] = {cuuint64_t(kBlk)};
+    const cuuint64_t out_dims[3] = {cuuint64_t(pe.rows), cuuint64_t(pe.cols), cuuint64_t(pe.e)};
+    const cuuint64_t out_strides[2] = {cuuint64_t(pe.rows), cuuint64_t(pe.rows * pe.cols)};
+    std::memset(in_map, 0, sizeof(CUtensorMap));
+    std::memset(out_map, 0, sizeof(CUtensorMap));
+    return enc(in_map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(blocks), in_dims, in_strides, box2,
+               one, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS &&
+           enc(out_map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, out, out_dims, out_strides, box3, one,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
 extern "C" int fp8z_transpose_fp8(const uint8_t* w_fp8, const float* inv_scale,
                                   const fp8z_param_entry* entry, uint8_t* out, float* inv_scale_t,
-                                  void* stream) {
+                                  int32_t* dev_status, void* stream) {
     if (!w_fp8 || !inv_scale || !entry || !out || !inv_scale_t) return FP8Z_EINVAL;
     const fp8z_param_entry& pe = *entry;
     if (pe.e < 1 || pe.rows < 1 || pe.cols < 1 || pe.blk_offset < 0) return FP8Z_EINVAL;
@@ -183,13 +314,35 @@ extern "C" int fp8z_transpose_fp8(const uint8_t* w_fp8, const float* inv_scale,
     const int64_t nb = pe.e * pe.hb * pe.wb;
     if (nb > 0x7FFFFFFFLL) return FP8Z_EINVAL;
     if (!host::aligned(w_fp8, 16) || !host::aligned(out, 16) || !host::aligned(inv_scale, 4) ||
-        !host::aligned(inv_scale_t, 4))
+        !host::aligned(inv_scale_t, 4) || !host::aligned(dev_status, 4))
         return FP8Z_EALIGN;
     int sms = 0;
-    const int rc = host::device_sms(&sms);
+    int rc = host::device_sms(&sms);
     if (rc != FP8Z_OK) return rc;
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const uint8_t* blocks = w_fp8 + pe.blk_offset * kBlkElems;
+    CUtensorMap in_map, out_map;
+    if (pe.rows % 16 == 0 && transpose_maps(pe, blocks, out, &in_map, &out_map)) {
+        rc = host::set_smem_once(reinterpret_cast<const void*>(&transpose_tma_kernel), 5, kTSmemBytes);
+        int per_sm = 0;
+        if (rc == FP8Z_OK)
+            rc = host::resident_ctas(reinterpret_cast<const void*>(&transpose_tma_kernel),
+                                     host::kResidentTransposeTma, 256, kTSmemBytes, &per_sm);
+        if (rc != FP8Z_OK) return rc;
+        const int64_t cap = int64_t(sms) * per_sm;
+        TransposeTmaArgs T;
+        T.inv = inv_scale + pe.blk_offset;
+        T.inv_t = inv_scale_t;
+        T.nb = nb;
+        T.hb = pe.hb;
+        T.wb = pe.wb;
+        T.dev_status = dev_status;
+        T.timeout_ns = host::kDefaultTimeoutNs;
+        transpose_tma_kernel<<<unsigned(nb < cap ? nb : cap), 256, kTSmemBytes, st>>>(in_map, out_map, T);
+        return cudaGetLastError() == cudaSuccess ? FP8Z_OK : FP8Z_ECUDA;
+    }
     TransposeArgs T;
-    T.q = w_fp8 + pe.blk_offset * kBlkElems;
+    T.q = blocks;
     T.inv = inv_scale + pe.blk_offset;
     T.out = out;
     T.inv_t = inv_scale_t;
@@ -197,7 +350,7 @@ extern "C" int fp8z_transpose_fp8(const uint8_t* w_fp8, const float* inv_scale,
     T.W = pe.cols;
     T.hb = pe.hb;
     T.wb = pe.wb;
-    transpose_kernel<<<unsigned(nb), 256, 0, static_cast<cudaStream_t>(stream)>>>(T);
+    transpose_kernel<<<unsigned(nb), 256, 0, st>>>(T);
     return cudaGetLastError() == cudaSuccess ? FP8Z_OK : FP8Z_ECUDA;
 }
 

@@ -122,6 +122,54 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
         : "memory");
 }
 
+// Tiled 2-D tensor-map load into shared memory (same rules as the 3-D one).
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(map), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
+// ------------------------------------------------------- bulk stores out
+// Shared -> global copies by the TMA engine, tracked in per-thread bulk
+// groups: commit after issuing, then wait before the shared source is reused
+// (the .read form returns once the engine has read the source).  Before the
+// copy, generic-proxy writes of the source must be fenced into the async proxy.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, int x, int y, int z, uint32_t src) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(map),
+        "r"(x), "r"(y), "r"(z), "r"(src)
+        : "memory");
+}
+
+__device__ __forceinline__ void bulk_s2g(void* dst, uint32_t src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+// Wait until at most N bulk groups of this thread still read shared memory.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+__device__ __forceinline__ void fence_proxy_async() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Byte offset of (row r, byte b) in a tile of 128-byte rows that a tensor map
+// with CU_TENSOR_MAP_SWIZZLE_128B loads or stores (tile 1024-byte aligned):
+// the 16-byte chunk index is XORed with r mod 8.
+__device__ __forceinline__ int swz128(int r, int b) {
+    return r * 128 + ((((b >> 4) ^ (r & 7)) << 4) | (b & 15));
+}
+
 // ------------------------------------------------------------- E4M3 cast
 // Two floats -> two E4M3 codes, round to nearest even, saturating to ±448
 // (NaN stays NaN).  `lo` lands in the low byte.

@@ -99,7 +99,7 @@ def lib():
         L.fp8z_adamw_requant_step_mx.argtypes = [P, P, P, P, P, P, i64, i64, i64, P,
                                                  ctypes.POINTER(fp8z_adamw_hparams), P, P]
         L.fp8z_dequant.argtypes = [P, P, i64, P, P]
-        L.fp8z_transpose_fp8.argtypes = [P, P, P, P, P, P]
+        L.fp8z_transpose_fp8.argtypes = [P, P, P, P, P, P, P]
         L.fp8z_fold.argtypes = [P, i32, P, P, P, P]
         L.fp8z_unfold.argtypes = [P, i32, P, P, P, P]
         L.fp8z_quantize_rowwise.argtypes = [P, i64, i64, i32, P, P, P]
@@ -284,9 +284,9 @@ def fp8z_dequant(w_fp8, inv_scale, nblk, out, stream=None):
     _check("fp8z_dequant", rc)
 
 
-def fp8z_transpose_fp8(w_fp8, inv_scale, entry, out, inv_scale_t, stream=None):
+def fp8z_transpose_fp8(w_fp8, inv_scale, entry, out, inv_scale_t, dev_status=None, stream=None):
     """entry: one param_entry_dtype record (host).  out: uint8 [E, W, H];
-    inv_scale_t: float32 [E, Wb, Hb]."""
+    inv_scale_t: float32 [E, Wb, Hb]; dev_status: optional int32 device word."""
     import torch
     ent = np.array([entry], dtype=param_entry_dtype)
     E, H, W = int(entry["e"]), int(entry["rows"]), int(entry["cols"])
@@ -299,7 +299,7 @@ def fp8z_transpose_fp8(w_fp8, inv_scale, entry, out, inv_scale_t, stream=None):
                                   _dptr(inv_scale, torch.float32, "inv_scale"), ent.ctypes.data,
                                   _dptr(out, torch.uint8, "out"),
                                   _dptr(inv_scale_t, torch.float32, "inv_scale_t"),
-                                  _stream_handle(stream))
+                                  _dptr(dev_status, torch.int32, "dev_status"), _stream_handle(stream))
     _check("fp8z_transpose_fp8", rc)
 
 
