@@ -19,34 +19,78 @@ constexpr int kBlkElems = FP8Z_BLOCK_ELEMS;
 
 // ------------------------------------------------------------- dequantize
 // "FP8-Flow-MoE" §3.1: D(Q(x)) = Q(x) * s, here value(code) * inv_scale.
-// HBM-bound (1 B read + 4 B written per element).  Each thread takes one
-// 32-bit word of codes (4 elements) per step, so a warp reads 128 contiguous
-// bytes of codes and writes 512 contiguous bytes of floats per instruction;
-// eight independent words per iteration keep loads in flight (with four the
-// kernel stalled on load latency: 71 % of DRAM peak).
-__global__ void __launch_bounds__(256) dequant_kernel(const uint32_t* __restrict__ q,
-                                                      const float* __restrict__ inv,
-                                                      int64_t nwords, float4* __restrict__ out) {
-    const int64_t stride = int64_t(gridDim.x) * blockDim.x;
-    constexpr int kU = 8;
-    for (int64_t w0 = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; w0 < nwords; w0 += kU * stride) {
-        uint32_t words[kU];
-        float s[kU];
+// HBM-bound (1 B read + 4 B written per element).  Persistent, one CTA per SM:
+// one thread streams each block's 16 KB of codes into a ring of kDqStages
+// shared buffers with bulk copies; the 1024 threads decode one 32-bit word of
+// codes each per pass (exact, cvt.rn.f16x2.e4m3x2, times the block's inverse
+// scale) into one of kDqOut 64 KB FP32 tiles; the thread writes the tile back
+// with one 64 KB bulk store.  Measured on GB300 (65,536 blocks): 0.966 of the
+// copy bandwidth, against 0.889 for a grid-stride kernel with 16-byte stores
+// (plain stores cap a 1:4 read:write stream near 0.92; bulk stores write at
+// 1.02 of the copy bandwidth).
+constexpr int kDqStages = 3, kDqOut = 2, kDqThreads = 1024;
+constexpr int kDqSmemBytes = kDqStages * kBlkElems + kDqOut * kBlkElems * 4 + kDqStages * 8 + 16;
+
+__global__ void __launch_bounds__(kDqThreads) dequant_kernel(const uint8_t* __restrict__ q,
+                                                             const float* __restrict__ inv, int64_t nblk,
+                                                             float* __restrict__ out, int32_t* dev_status,
+                                                             int64_t timeout_ns) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    unsigned char* codes = smem;                                              // kDqStages x 16 KB
+    float* tiles = reinterpret_cast<float*>(smem + kDqStages * kBlkElems);   // kDqOut x 64 KB
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kDqStages * kBlkElems + kDqOut * kBlkElems * 4);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + kDqStages);
+    const int tid = threadIdx.x;
+    const uint32_t bar0 = smem_addr(bars);
+    if (tid == 0) {
+        for (int s = 0; s < kDqStages; ++s) mbar_init(bar0 + 8 * s, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    const Watchdog wd{abort_flag, dev_status, timeout_ns};
+    const int64_t count = (nblk - blockIdx.x + gridDim.x - 1) / gridDim.x;   // grid <= nblk
+    auto issue = [&](int64_t k) {
+        const int64_t b = blockIdx.x + k * gridDim.x;
+        const int s = int(k % kDqStages);
+        mbar_arrive_expect_tx(bar0 + 8 * s, kBlkElems);
+        bulk_g2s_nohint(smem_addr(codes + s * kBlkElems), q + b * kBlkElems, kBlkElems, bar0 + 8 * s);
+    };
+    if (tid == 0)
+        for (int64_t k = 0; k < count && k < kDqStages; ++k) issue(k);
+    int64_t k = 0;
+    for (; k < count; ++k) {
+        const int64_t b = blockIdx.x + k * gridDim.x;
+        const int s = int(k % kDqStages), ot = int(k % kDqOut);
+        if (tid == 0) bulk_wait_read<kDqOut - 1>();        // tile ot has been written out
+        mbar_wait_bounded(bar0 + 8 * s, uint32_t((k / kDqStages) & 1), wd);
+        __syncthreads();
+        if (*abort_flag) break;
+        const float sc = __ldg(inv + b);
+        const uint32_t* cw = reinterpret_cast<const uint32_t*>(codes + s * kBlkElems);
+        float4* t4 = reinterpret_cast<float4*>(tiles + ot * kBlkElems);
 #pragma unroll
-        for (int u = 0; u < kU; ++u) {
-            const int64_t w = w0 + u * stride;
-            words[u] = w < nwords ? __ldcs(q + w) : 0u;
-            s[u] = w < nwords ? __ldg(inv + (w >> 12)) : 0.0f;   // 4096 words per block
+        for (int it = 0; it < kBlkElems / 4 / kDqThreads; ++it) {
+            const int w = it * kDqThreads + tid;
+            const uint32_t word = cw[w];
+            const float2 lo = e4m3x2_to_float2(word);
+            const float2 hi = e4m3x2_to_float2(word >> 16);
+            t4[w] = make_float4(__fmul_rn(lo.x, sc), __fmul_rn(lo.y, sc), __fmul_rn(hi.x, sc),
+                                __fmul_rn(hi.y, sc));
         }
-#pragma unroll
-        for (int u = 0; u < kU; ++u) {
-            const int64_t w = w0 + u * stride;
-            if (w >= nwords) break;
-            const float2 a = e4m3x2_to_float2(words[u]);
-            const float2 b = e4m3x2_to_float2(words[u] >> 16);
-            __stcs(out + w, make_float4(__fmul_rn(a.x, s[u]), __fmul_rn(a.y, s[u]),
-                                        __fmul_rn(b.x, s[u]), __fmul_rn(b.y, s[u])));
+        fence_proxy_async();
+        __syncthreads();
+        if (tid == 0) {
+            bulk_s2g(out + b * kBlkElems, smem_addr(tiles + ot * kBlkElems), kBlkElems * 4);
+            bulk_commit();
+            if (k + kDqStages < count) issue(k + kDqStages);
         }
+    }
+    if (tid == 0) {
+        if (k < count)                                     // gave up: let the issued loads land
+            for (int64_t kk = k; kk < count && kk < k + kDqStages; ++kk)
+                mbar_wait_bounded(bar0 + 8 * int(kk % kDqStages), uint32_t((kk / kDqStages) & 1), wd, false);
+        bulk_wait_all();
     }
 }
 
@@ -253,24 +297,21 @@ int grid_for(int64_t work, int per_sm) {
 using namespace fp8z;
 
 extern "C" int fp8z_dequant(const uint8_t* w_fp8, const float* inv_scale, int64_t nblk, float* out,
-                            void* stream) {
+                            int32_t* dev_status, void* stream) {
     if (!w_fp8 || !inv_scale || !out || nblk < 0) return FP8Z_EINVAL;
     if (nblk > (INT64_MAX / kBlkElems) / 4) return FP8Z_EINVAL;
-    if (!host::aligned(w_fp8, 16) || !host::aligned(out, 16) || !host::aligned(inv_scale, 4))
+    if (!host::aligned(w_fp8, 16) || !host::aligned(out, 16) || !host::aligned(inv_scale, 4) ||
+        !host::aligned(dev_status, 4))
         return FP8Z_EALIGN;
     if (nblk == 0) return FP8Z_OK;
-    int sms = 0, per_sm = 0;
+    int sms = 0;
     int rc = host::device_sms(&sms);
     if (rc != FP8Z_OK) return rc;
-    rc = host::resident_ctas(reinterpret_cast<const void*>(&dequant_kernel), host::kResidentDequant, 256, 0,
-                             &per_sm);
+    rc = host::set_smem_once(reinterpret_cast<const void*>(&dequant_kernel), 6, kDqSmemBytes);
     if (rc != FP8Z_OK) return rc;
-    const int64_t nwords = nblk * (kBlkElems / 4);
-    const int64_t want = (nwords + 2047) / 2048;
-    const int64_t cap = int64_t(sms) * per_sm;      // one wave: 8 per SM would be 1.3 waves (+3.5 %)
-    const unsigned grid = unsigned(want < cap ? want : cap);
-    dequant_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(
-        reinterpret_cast<const uint32_t*>(w_fp8), inv_scale, nwords, reinterpret_cast<float4*>(out));
+    const unsigned grid = unsigned(nblk < sms ? nblk : sms);
+    dequant_kernel<<<grid, kDqThreads, kDqSmemBytes, static_cast<cudaStream_t>(stream)>>>(
+        w_fp8, inv_scale, nblk, out, dev_status, host::kDefaultTimeoutNs);
     return cudaGetLastError() == cudaSuccess ? FP8Z_OK : FP8Z_ECUDA;
 }
 

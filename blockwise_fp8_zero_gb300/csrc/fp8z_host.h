@@ -41,7 +41,7 @@ int set_smem_once(const void* kernel, int slot, int bytes);
 // device).  Grid-stride kernels launch exactly SMs x this many CTAs: a grid
 // that does not fit in one wave leaves its last CTAs running alone.
 int resident_ctas(const void* kernel, int slot, int threads, int smem, int* per_sm);
-enum ResidentSlot { kResidentQuantizeRowwise = 0, kResidentDequant = 1, kResidentTransposeTma = 2 };
+enum ResidentSlot { kResidentQuantizeRowwise = 0, kResidentTransposeTma = 1 };
 
 // The driver's cuTensorMapEncodeTiled (through the runtime's entry-point
 // query, so the library needs no link against libcuda); nullptr if absent.

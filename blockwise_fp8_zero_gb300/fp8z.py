@@ -98,7 +98,7 @@ def lib():
         L.fp8z_encode_grad_maps.argtypes = [P, P, i32, P]
         L.fp8z_adamw_requant_step_mx.argtypes = [P, P, P, P, P, P, i64, i64, i64, P,
                                                  ctypes.POINTER(fp8z_adamw_hparams), P, P]
-        L.fp8z_dequant.argtypes = [P, P, i64, P, P]
+        L.fp8z_dequant.argtypes = [P, P, i64, P, P, P]
         L.fp8z_transpose_fp8.argtypes = [P, P, P, P, P, P, P]
         L.fp8z_fold.argtypes = [P, i32, P, P, P, P]
         L.fp8z_unfold.argtypes = [P, i32, P, P, P, P]
@@ -274,13 +274,14 @@ def fp8z_adamw_requant_step_rowmajor(p, m, v, g_maps, w_row, inv_scale, blk_begi
     _check("fp8z_adamw_requant_step_rowmajor", rc)
 
 
-def fp8z_dequant(w_fp8, inv_scale, nblk, out, stream=None):
+def fp8z_dequant(w_fp8, inv_scale, nblk, out, dev_status=None, stream=None):
     import torch
     if w_fp8.numel() < nblk * BLOCK_ELEMS or out.numel() < nblk * BLOCK_ELEMS or inv_scale.numel() < nblk:
         raise ValueError("buffers smaller than nblk blocks")
     rc = lib().fp8z_dequant(_dptr(w_fp8, torch.uint8, "w_fp8"),
                             _dptr(inv_scale, torch.float32, "inv_scale"), int(nblk),
-                            _dptr(out, torch.float32, "out"), _stream_handle(stream))
+                            _dptr(out, torch.float32, "out"), _dptr(dev_status, torch.int32, "dev_status"),
+                            _stream_handle(stream))
     _check("fp8z_dequant", rc)
 
 

@@ -253,10 +253,13 @@ FP8Z_API int fp8z_encode_grad_maps(const void *const *g_ptrs, const fp8z_param_e
  * fp8z_dequant -- out[b][i] = E4M3_value(w_fp8[b][i]) * inv_scale[b] (float
  * product), for nblk blocks ("FP8-Flow-MoE" §3.1, D(Q(x)) = Q(x)*s).
  * w_fp8: device u8 [nblk,128,128]; inv_scale: device f32 [nblk];
- * out: device f32 [nblk,128,128].  Returns FP8Z_OK / EINVAL / EALIGN / ECUDA.
+ * out: device f32 [nblk,128,128]; w_fp8 and out 16-byte aligned (they move
+ * through the TMA engine as whole blocks).  dev_status: nullable device
+ * int32, 4-byte aligned; FP8Z_ETIMEOUT lands there if a bounded wait gave up.
+ * Returns FP8Z_OK / EINVAL / EALIGN / ECUDA.
  */
 FP8Z_API int fp8z_dequant(const uint8_t *w_fp8, const float *inv_scale, int64_t nblk,
-                 float *out, void *stream);
+                 float *out, int32_t *dev_status, void *stream);
 
 /*
  * fp8z_transpose_fp8 -- column-major copy of one quantized param.  With

@@ -135,10 +135,11 @@ def test_step_argument_errors(L):
 
 
 def test_aux_argument_errors(L):
-    assert L.fp8z_dequant(None, A16, 1, A16, None) == fp8z.FP8Z_EINVAL
-    assert L.fp8z_dequant(A4, A16, 1, A16, None) == fp8z.FP8Z_EALIGN
-    assert L.fp8z_dequant(A16, A16, -1, A16, None) == fp8z.FP8Z_EINVAL
-    assert L.fp8z_dequant(A16, A16, 0, A16, None) == fp8z.FP8Z_OK
+    assert L.fp8z_dequant(None, A16, 1, A16, None, None) == fp8z.FP8Z_EINVAL
+    assert L.fp8z_dequant(A4, A16, 1, A16, None, None) == fp8z.FP8Z_EALIGN
+    assert L.fp8z_dequant(A16, A16, 1, A16, A16 + 2, None) == fp8z.FP8Z_EALIGN
+    assert L.fp8z_dequant(A16, A16, -1, A16, None, None) == fp8z.FP8Z_EINVAL
+    assert L.fp8z_dequant(A16, A16, 0, A16, None, None) == fp8z.FP8Z_OK
     ent = np.zeros(1, fp8z.param_entry_dtype)
     ent[0] = (0, 0, 0, 1, 200, 300, 2, 2, 0, 0)                  # wb should be 3
     assert L.fp8z_transpose_fp8(A16, A16, ent.ctypes.data, A16, A16, None, None) == fp8z.FP8Z_EINVAL

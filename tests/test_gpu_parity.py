@@ -205,6 +205,25 @@ def test_dequant(oracle):
     assert np.array_equal(out.cpu().numpy().view(np.uint32), want.view(np.uint32))
 
 
+@pytest.mark.parametrize("nblk", [1, 153, 2000])
+def test_dequant_every_code(oracle, nblk):
+    # every finite code and its negation, spread over many blocks per persistent
+    # CTA, each block with its own inverse scale (powers of two and not)
+    rng = np.random.default_rng(nblk)
+    codes = rng.integers(0, 256, nblk * BLK, dtype=np.uint8)
+    codes[(codes & 0x7F) == 0x7F] = 0x00                      # NaN codes: never produced by the step
+    codes[:254] = [c for c in range(256) if (c & 0x7F) != 0x7F]
+    inv = (rng.uniform(0.5, 2.0, nblk) * 2.0 ** rng.integers(-20, 20, nblk)).astype(np.float32)
+    inv[::3] = 2.0 ** rng.integers(-30, 30, inv[::3].size).astype(np.float32)
+    out = torch.full((nblk * BLK,), float("nan"), dtype=torch.float32, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    fp8z.fp8z_dequant(torch.from_numpy(codes).cuda(), torch.from_numpy(inv).cuda(), nblk, out, dev_status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    want = oracle.dequant(codes, inv, nblk)
+    assert np.array_equal(out.cpu().numpy().view(np.uint32), want.view(np.uint32))
+
+
 # rows a multiple of 16 take the TMA kernel (ragged edges clipped by the
 # tensor-map store, several blocks per persistent CTA), the rest the plain one
 @pytest.mark.parametrize("shape", [(1, 384, 640), (2, 300, 260), (1, 129, 1), (3, 7168 // 28, 576),
