@@ -73,6 +73,20 @@ def test_ragged_shapes(oracle, shapes, transposed):
     assert_bitexact(c.results(), c.oracle(oracle, hp), c.processed)
 
 
+# Larger shards with the column-major copy, fully checked: whole expert
+# matrices with more block columns than CTAs (several blocks per CTA), a wide
+# ragged param (hb = 3, wb = 201), whole params per param-wise bucket, and
+# block-wise shards that cut an expert matrix.
+@pytest.mark.parametrize("shapes,dp,split", [([(4, 1024, 5120)], 1, 0), ([(1, 256, 38400)], 1, 0),
+                                             ([(2, 512, 10240), (2, 512, 10240)], 2, 1),
+                                             ([(1, 300, 25700)], 1, 0), ([(1, 256, 38400)], 3, 0)])
+def test_larger_shards_with_copy(oracle, shapes, dp, split):
+    c = Case(shapes, dp=dp, split=split, seed=dp + len(shapes), transposed=True)
+    hp = fp8z.hparams(step=4)
+    c.step(hp)
+    assert_bitexact(c.results(), c.oracle(oracle, hp), c.processed)
+
+
 @pytest.mark.parametrize("kw", [dict(step=1), dict(step=1000), dict(decay_mode=1, step=5),
                                 dict(scale_mode=1, step=3), dict(lr=3e-3, weight_decay=0.0, step=2),
                                 dict(beta1=0.0, beta2=0.0, step=7), dict(min_scale=1e3, step=2)])
