@@ -586,49 +586,49 @@ __global__ void __launch_bounds__(kThreads, 1) fp8z_step_kernel(const StepArgs A
                 staged = false;
             }
         }
-        if constexpr (kMx) continue;
-
-        // ---- block amax: warp shuffle, then one exchange through shared memory
+        if constexpr (!kMx) {       // MXFP8 blocks are complete after their stages
+            // ---- block amax: warp shuffle, then one exchange through shared memory
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) lmax = fmaxf(lmax, __shfl_xor_sync(0xFFFFFFFFu, lmax, o));
-        float* ax = amax_x + (i & 1) * kConsumerWarps;
-        if (lane == 0) {
-            ax[warp] = lmax;
-            mbar_arrive(amax_bar);
-        }
-        if (!mbar_wait_bounded(amax_bar, uint32_t(i & 1), wd)) return;
-        float amax = ax[0];
-#pragma unroll
-        for (int w = 1; w < kConsumerWarps; ++w) amax = fmaxf(amax, ax[w]);
-
-        const float s = block_scale(A, amax);
-        const float inv = __fdiv_rn(1.0f, s);
-        if (tid == 0) A.inv_scale[blk] = inv;
-
-        // ---- quantize the kept p' and store the E4M3 block
-        uint32_t words[kKeep];
-#pragma unroll
-        for (int k = 0; k < kKeep; ++k) {
-            const float4 x = keep[k];
-            words[k] = pack_e4m3x4(__fmul_rn(x.x, s), __fmul_rn(x.y, s), __fmul_rn(x.z, s),
-                                   __fmul_rn(x.w, s));
-            if (!kRowMajor) {
-                const int row = k * kConsumerWarps + warp;
-                store_word(A.w_fp8 + base + size_t(row) * kBlk + col, words[k]);
+            for (int o = 16; o > 0; o >>= 1) lmax = fmaxf(lmax, __shfl_xor_sync(0xFFFFFFFFu, lmax, o));
+            float* ax = amax_x + (i & 1) * kConsumerWarps;
+            if (lane == 0) {
+                ax[warp] = lmax;
+                mbar_arrive(amax_bar);
             }
-        }
-        const BlockInfo bi = c->bi;
-        const ParamInfo pi = c->pi;
-        if (kRowMajor && bi.param >= 0) {
-            if (dest_ok(A, bi, pi, A.w_row_bytes, -1))
-                store_rowmajor(A, bi, pi, words, warp, col);
-            else if (tid == 0)
-                report_status(A.dev_status, FP8Z_EINVAL);
-        }
+            if (!mbar_wait_bounded(amax_bar, uint32_t(i & 1), wd)) return;
+            float amax = ax[0];
+#pragma unroll
+            for (int w = 1; w < kConsumerWarps; ++w) amax = fmaxf(amax, ax[w]);
 
-        // ---- optional column-major copy of the param + transposed scale grid
-        if (transposed && bi.param >= 0) {
-            staged = column_major_in(A, bi, pi, words, inv, tile, tile_bar, tid, warp, lane);
+            const float s = block_scale(A, amax);
+            const float inv = __fdiv_rn(1.0f, s);
+            if (tid == 0) A.inv_scale[blk] = inv;
+
+            // ---- quantize the kept p' and store the E4M3 block
+            uint32_t words[kKeep];
+#pragma unroll
+            for (int k = 0; k < kKeep; ++k) {
+                const float4 x = keep[k];
+                words[k] = pack_e4m3x4(__fmul_rn(x.x, s), __fmul_rn(x.y, s), __fmul_rn(x.z, s),
+                                       __fmul_rn(x.w, s));
+                if (!kRowMajor) {
+                    const int row = k * kConsumerWarps + warp;
+                    store_word(A.w_fp8 + base + size_t(row) * kBlk + col, words[k]);
+                }
+            }
+            const BlockInfo bi = c->bi;
+            const ParamInfo pi = c->pi;
+            if (kRowMajor && bi.param >= 0) {
+                if (dest_ok(A, bi, pi, A.w_row_bytes, -1))
+                    store_rowmajor(A, bi, pi, words, warp, col);
+                else if (tid == 0)
+                    report_status(A.dev_status, FP8Z_EINVAL);
+            }
+
+            // ---- optional column-major copy of the param + transposed scale grid
+            if (transposed && bi.param >= 0) {
+                staged = column_major_in(A, bi, pi, words, inv, tile, tile_bar, tid, warp, lane);
+            }
         }
     }
     if (staged) {
