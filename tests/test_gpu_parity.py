@@ -124,6 +124,49 @@ def test_special_blocks(oracle):
     assert_bitexact(c.results(), c.oracle(oracle, hp), c.processed)
 
 
+def _random_hparams(rng):
+    return dict(lr=float(10 ** rng.uniform(-7, -1)), beta1=float(rng.choice([0.0, rng.uniform(0, 0.99)])),
+                beta2=float(rng.choice([0.0, rng.uniform(0, 0.9999)])), eps=float(10 ** rng.uniform(-12, -2)),
+                weight_decay=float(rng.choice([0.0, rng.uniform(0, 1)])),
+                step=int(10 ** rng.uniform(0, 6)), scale_mode=int(rng.integers(0, 2)),
+                decay_mode=int(rng.integers(0, 2)),
+                fp8_max=float(rng.choice([448.0, 240.0, 1.0 + rng.uniform(0, 447)])),
+                min_scale=float(rng.choice([0.0, 1e-6, rng.uniform(0, 1e3)])))
+
+
+@pytest.mark.parametrize("seed", range(24))
+def test_hyperparameter_sweep(oracle, seed):
+    """Seeded random hyper-parameters (every field the step reads, both scale
+    and decay modes, steps up to 1e6) on a ragged two-param, two-shard layout
+    with the column-major copy: the same bits as the oracle."""
+    rng = np.random.default_rng(1000 + seed)
+    c = Case([(1, 200, 300), (2, 130, 129)], dp=2, seed=seed, transposed=True)
+    hp = fp8z.hparams(**_random_hparams(rng))
+    c.step(hp)
+    assert_bitexact(c.results(), c.oracle(oracle, hp), c.processed)
+
+
+@pytest.mark.parametrize("scale_mode", [0, 1])
+def test_extreme_magnitudes(oracle, scale_mode):
+    """State and grads log-uniform over [1e-42, 1e38] with random signs (v kept
+    >= 0), exact zeros mixed in: subnormal operands, g*g overflowing to Inf,
+    quotients overflowing, blocks whose amax is subnormal or near FLT_MAX."""
+    c = Case([(1, 256, 640)], dp=1, seed=9, transposed=True)
+    rng = np.random.default_rng(77 + scale_mode)
+    for k in "pgmv":
+        n = c.host[k].size
+        mag = 10.0 ** rng.uniform(-42, 38, n)
+        x = (mag * rng.choice([-1.0, 1.0], n)).astype(np.float32)
+        x[rng.random(n) < 0.02] = 0.0
+        if k == "v":
+            x = np.abs(x)
+        c.host[k][:] = x
+        c.dev[k].copy_(torch.from_numpy(c.host[k]))
+    hp = fp8z.hparams(step=7, scale_mode=scale_mode)
+    c.step(hp)
+    assert_bitexact(c.results(), c.oracle(oracle, hp), c.processed)
+
+
 def test_shard_launches_equal_one_launch(oracle):
     shapes = [(1, 640, 384), (2, 200, 300), (1, 128, 1000)]
     hp = fp8z.hparams(step=6)
