@@ -29,10 +29,12 @@ namespace {
 
 constexpr int kTile = FP8Z_BLOCK;         // 128 elements per scale
 // Exponent k of the smallest power of two >= amax/448 (exact, from the bits
-// of amax > 0), kept in the normal float range [-126, 127].  448 = 1.75 * 2^8,
-// so with amax = m * 2^e (m in [1, 2)) the answer is e-8, or e-7 when m > 1.75.
+// of amax > 0), kept in the normal float range [-126, 127]; an infinite amax
+// takes the clamp, 127.  448 = 1.75 * 2^8, so with amax = m * 2^e (m in [1, 2))
+// the answer is e-8, or e-7 when m > 1.75.
 __device__ __forceinline__ int pow2_tile_exponent(float amax) {
     const uint32_t b = __float_as_uint(amax);
+    if ((b >> 23) == 255) return 127;     // +Inf (a NaN never becomes the amax)
     int e;
     uint32_t man;
     if ((b >> 23) == 0) {                 // subnormal: normalise

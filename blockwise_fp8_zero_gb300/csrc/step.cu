@@ -185,10 +185,11 @@ __device__ __forceinline__ int64_t imin64(int64_t a, int64_t b) { return a < b ?
 
 // MXFP8 shared exponent of a group with largest magnitude a: floor(log2 a) - 8
 // (8 = the largest E4M3 exponent, so the largest element lands in [256, 512)),
-// clamped to [-127, 127]; 0 for an all-zero group.
+// clamped to [-127, 127]; 0 for an all-zero group, 127 for an infinite amax.
 __device__ __forceinline__ int mx_exponent(float a) {
     if (a == 0.0f) return 0;
     const uint32_t b = __float_as_uint(a);
+    if ((b >> 23) == 255) return 127;     // +Inf (a NaN never becomes the amax)
     const int e = (b >> 23) == 0 ? (31 - __clz(b)) - 149 : int(b >> 23) - 127;
     const int x = e - 8;
     return x < -127 ? -127 : (x > 127 ? 127 : x);

@@ -708,9 +708,12 @@ void fp8z_ref_quantize_rowwise(const float *x, int64_t R, int64_t C, int pow2,
                 /* smallest 2^k >= amax/448, on the exact quotient, kept within
                  * the normal float range [2^-126, 2^127] */
                 double ratio = (double)amax / 448.0;
-                int e;
-                double f = frexp(ratio, &e);          /* ratio = f * 2^e, f in [0.5,1) */
-                int k = (f == 0.5) ? e - 1 : e;
+                int k = 127;                          /* an infinite amax takes the clamp (READING) */
+                if (!isinf(ratio)) {
+                    int e;
+                    double f = frexp(ratio, &e);      /* ratio = f * 2^e, f in [0.5,1) */
+                    k = (f == 0.5) ? e - 1 : e;
+                }
                 if (k < -126) k = -126;
                 if (k > 127) k = 127;
                 sc = ldexp(1.0, k);
@@ -817,7 +820,9 @@ int fp8z_ref_adamw_requant_step_mx(float *p, const float *g, float *m, float *v,
                 for (int c = 0; c < 32; ++c)
                     amax = fmaxf(amax, fabsf(row[gi * 32 + c]));
                 int ex = 0;
-                if (amax > 0.0f) {
+                if (isinf(amax)) {
+                    ex = 127;                           /* floor(log2(+Inf)) - 8, clamped (READING) */
+                } else if (amax > 0.0f) {
                     int e2;
                     (void)frexp((double)amax, &e2);     /* amax = f * 2^e2, f in [0.5,1) */
                     ex = (e2 - 1) - 8;

@@ -386,3 +386,34 @@ def test_mxfp8_step(oracle, shapes):
     assert np.array_equal(c.w_fp8.cpu().numpy(), q)
     data = np.repeat(c.blocks["param"] >= 0, 512)
     assert np.array_equal(mx.cpu().numpy()[data], sc[data])
+
+
+@pytest.mark.parametrize("step", [1, 50])
+def test_mxfp8_extreme_magnitudes(oracle, step):
+    """The MXFP8 step on state and grads spread over [1e-42, 1e38] (zeros mixed
+    in): groups whose amax is subnormal, near FLT_MAX or zero; bit for bit."""
+    c = Case([(1, 256, 384)], dp=1, seed=23)
+    rng = np.random.default_rng(step)
+    for k in "pgmv":
+        n = c.host[k].size
+        x = (10.0 ** rng.uniform(-42, 38, n) * rng.choice([-1.0, 1.0], n)).astype(np.float32)
+        x[rng.random(n) < 0.02] = 0.0
+        c.host[k][:] = np.abs(x) if k == "v" else x
+        c.dev[k].copy_(torch.from_numpy(c.host[k]))
+    hp = fp8z.hparams(step=step)
+    mx = torch.zeros(c.cap * 512, dtype=torch.uint8, device="cuda")
+    fp8z.fp8z_adamw_requant_step_mx(c.dev["p"], c.dev["g"], c.dev["m"], c.dev["v"], c.w_fp8, mx, 0, c.cap, hp,
+                                    desc=c.desc_dev, dev_status=c.status)
+    torch.cuda.synchronize()
+    assert c.status.item() == 0
+    p, g, m, v = (c.host[k].copy() for k in "pgmv")
+    q = np.zeros(c.cap * BLK, np.uint8)
+    sc = np.zeros(c.cap * 512, np.uint8)
+    oracle.adamw_requant_step_mx(p, g, m, v, q, sc, 0, c.cap, oracle.Hparams.make(step=step),
+                                 desc=np.ascontiguousarray(c.blocks).view(oracle.BLOCK_DESC))
+    for k, want in (("p", p), ("m", m), ("v", v)):
+        a = c.dev[k].cpu().numpy()
+        assert np.all((a.view(np.uint32) == want.view(np.uint32)) | (np.isnan(a) & np.isnan(want))), k
+    qa = c.w_fp8.cpu().numpy()
+    assert np.all((qa == q) | (((qa & 0x7F) == 0x7F) & ((q & 0x7F) == 0x7F)))
+    assert np.array_equal(mx.cpu().numpy(), sc)

@@ -77,3 +77,30 @@ def test_rowwise_argument_errors():
         fp8z.fp8z_transpose_rowwise(q, torch.ones(100, 1, device="cuda"),
                                     torch.empty(128, 100, dtype=torch.uint8, device="cuda"),
                                     torch.empty(128, 1, device="cuda"))
+
+
+@pytest.mark.parametrize("pow2", [True, False])
+def test_rowwise_extreme_magnitudes(oracle, pow2):
+    """Activations log-uniform over [1e-42, 1e38] with random signs and whole
+    zero tiles: tiles whose amax is subnormal or near FLT_MAX, scales at both
+    clamps; quantizer and scaling-aware transpose bit for bit."""
+    rng = np.random.default_rng(int(pow2))
+    R, C = 512, 640
+    x = (10.0 ** rng.uniform(-42, 38, (R, C)) * rng.choice([-1.0, 1.0], (R, C))).astype(np.float32)
+    x[rng.random((R, C)) < 0.02] = 0.0
+    x[5, 128:256] = 0.0
+    x[9] *= 1e-30                                  # a row of subnormal-range values
+    if pow2:
+        x[11, 200] = np.inf                        # an infinite tile amax takes the clamp
+        x[12, 3] = -np.inf
+    q, s = _gpu_quantize(torch.from_numpy(x), pow2)
+    qt = torch.empty(C, R, dtype=torch.uint8, device="cuda")
+    st = torch.empty(C, R // 128, device="cuda")
+    fp8z.fp8z_transpose_rowwise(q, s, qt, st)
+    torch.cuda.synchronize()
+    qo, so = oracle.quantize_rowwise(x, pow2=pow2)
+    assert np.array_equal(s.cpu().numpy().view(np.uint32), so.view(np.uint32))
+    assert np.array_equal(q.cpu().numpy(), qo)
+    qto, sto = oracle.transpose_rowwise(qo, so)
+    assert np.array_equal(st.cpu().numpy().view(np.uint32), sto.view(np.uint32))
+    assert np.array_equal(qt.cpu().numpy(), qto)

@@ -70,6 +70,38 @@ def test_mx_spike_only_moves_its_group(oracle):
     assert list(changed) == [5 * 4 + 1]                    # row 5, group 1 only
 
 
+def test_mx_infinite_amax(oracle):
+    """An infinite p' makes its group's amax +Inf: floor(log2 amax) - 8 is then
+    +Inf, clamped to 127 (scale byte 254); the Inf element saturates to the
+    +-448 code, the group's finite elements (|p'| << 2^127) round to a signed
+    zero, and every other group keeps the finite rule."""
+    rng = np.random.default_rng(3)
+    p, g, m, v = _state(rng, 1, spike=False)
+    p[7 * 128 + 70] = np.inf                 # row 7, group 2
+    p[9 * 128 + 3] = -np.inf                 # row 9, group 0
+    q = np.zeros(BLK, np.uint8)
+    sc = np.zeros(512, np.uint8)
+    ref = [x.copy() for x in (p, g, m, v)]
+    oracle.adamw_requant_step_mx(p, g, m, v, q, sc, 0, 1, oracle.Hparams.make(step=3))
+    assert sc[7 * 4 + 2] == 254 and sc[9 * 4 + 0] == 254
+    assert q[7 * 128 + 70] == 0x7E and q[9 * 128 + 3] == 0xFE
+    for r, gi in ((7, 2), (9, 0)):
+        grp = q[r * 128 + gi * 32:r * 128 + gi * 32 + 32]
+        fin = np.isfinite(p[r * 128 + gi * 32:r * 128 + gi * 32 + 32])
+        assert np.all((grp[fin] & 0x7F) == 0)
+    # the other groups: same bytes as a run without the infinities
+    p0, g0, m0, v0 = ref
+    p0[7 * 128 + 70] = 0.0
+    p0[9 * 128 + 3] = 0.0
+    q0 = np.zeros(BLK, np.uint8)
+    s0 = np.zeros(512, np.uint8)
+    oracle.adamw_requant_step_mx(p0, g0, m0, v0, q0, s0, 0, 1, oracle.Hparams.make(step=3))
+    keep = np.ones(512, bool)
+    keep[[7 * 4 + 2, 9 * 4 + 0]] = False
+    assert np.array_equal(sc[keep], s0[keep])
+    assert np.array_equal(q.reshape(512, 32)[keep], q0.reshape(512, 32)[keep])
+
+
 def test_mx_padding_and_desc(oracle):
     shapes = [(1, 200, 100)]                                # ragged rows and cols
     params, shards, blocks, summ = oracle.plan_shards(shapes, 1, 0)

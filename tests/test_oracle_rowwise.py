@@ -138,3 +138,26 @@ def test_double_quantization_error(oracle):
     assert np.all((E - D)[moved] < 1)                 # only underflowed values move
     assert np.mean(moved) < 0.01 and np.mean(naive != v_row.T) < 0.01
     assert abs(rel(direct) - rel(ref)) < 1e-3 * rel(ref)
+
+
+def test_infinite_tile_amax_takes_the_clamp(oracle):
+    """Power-of-two scales: a tile holding an Inf has amax/448 = Inf, whose
+    smallest power of two above it is out of range: the scale is the clamp,
+    2^127; the Inf saturates to the +-448 code and the finite values round to
+    a signed zero.  Other tiles keep the finite rule."""
+    rng = np.random.default_rng(8)
+    x = _act(rng, 4, 384, outliers=False)
+    x[1, 130] = np.inf
+    x[2, 300] = -np.inf
+    q, s = oracle.quantize_rowwise(x, pow2=True)
+    assert s[1, 1] == np.float32(2.0 ** 127) and s[2, 2] == np.float32(2.0 ** 127)
+    assert q[1, 130] == 0x7E and q[2, 300] == 0xFE
+    fin = np.isfinite(x[1, 128:256])
+    assert np.all((q[1, 128:256][fin] & 0x7F) == 0)
+    x0 = x.copy()
+    x0[1, 130] = 0.0
+    x0[2, 300] = 0.0
+    q0, s0 = oracle.quantize_rowwise(x0, pow2=True)
+    keep = np.ones_like(s, bool)
+    keep[1, 1] = keep[2, 2] = False
+    assert np.array_equal(s[keep], s0[keep])
