@@ -24,7 +24,7 @@ def _lib():
     fp8z.lib()
 
 
-def run_case(oracle, shapes, dp, split=0, transposed=False, step=5, seed=0, bad_desc=False):
+def run_case(oracle, shapes, dp, split=0, transposed=False, step=5, seed=0, bad_desc=False, hp_kw=None):
     params, shards, blocks, summ = fp8z.fp8z_plan_shards(shapes, dp, split)
     cap = int(summ["capacity_blocks"])
     dev = torch.device("cuda")
@@ -58,7 +58,7 @@ def run_case(oracle, shapes, dp, split=0, transposed=False, step=5, seed=0, bad_
     desc = fp8z.table_to_device(bl)
     pdev = fp8z.table_to_device(params)
     st = torch.zeros(1, dtype=torch.int32, device=dev)
-    hp = fp8z.hparams(step=step)
+    hp = fp8z.hparams(**(hp_kw or {"step": step}))
     for s in shards:
         fp8z.fp8z_adamw_requant_step_rowmajor(d["p"], d["m"], d["v"], maps, w_row, inv,
                                               int(s["blk_begin"]), int(s["blk_count_real"]), hp,
@@ -103,6 +103,19 @@ def test_rowmajor_step(oracle, shapes, transposed):
 def test_rowmajor_step_extreme_shapes(oracle, shapes):
     # a 256 KB grad row pitch, 513 block rows, 512 one-block experts
     run_case(oracle, shapes, dp=1, transposed=True, seed=11)
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_rowmajor_step_hyperparameters(oracle, seed):
+    # random hyper-parameters (every field the step reads) on a ragged layout
+    rng = np.random.default_rng(500 + seed)
+    hp_kw = dict(lr=float(10 ** rng.uniform(-7, -1)), beta1=float(rng.uniform(0, 0.99)),
+                 beta2=float(rng.uniform(0, 0.9999)), eps=float(10 ** rng.uniform(-12, -2)),
+                 weight_decay=float(rng.uniform(0, 1)), step=int(10 ** rng.uniform(0, 6)),
+                 scale_mode=int(rng.integers(0, 2)), decay_mode=int(rng.integers(0, 2)),
+                 fp8_max=float(rng.choice([448.0, 1.0 + rng.uniform(0, 447)])),
+                 min_scale=float(rng.choice([0.0, 1e-6, rng.uniform(0, 1e3)])))
+    run_case(oracle, [(1, 300, 200), (2, 128, 260)], dp=2, transposed=True, seed=seed, hp_kw=hp_kw)
 
 
 @pytest.mark.parametrize("split", [0, 1])
