@@ -417,3 +417,31 @@ def test_mxfp8_extreme_magnitudes(oracle, step):
     qa = c.w_fp8.cpu().numpy()
     assert np.all((qa == q) | (((qa & 0x7F) == 0x7F) & ((q & 0x7F) == 0x7F)))
     assert np.array_equal(mx.cpu().numpy(), sc)
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_mxfp8_hyperparameters(oracle, seed):
+    """The MXFP8 step under random hyper-parameters (the AdamW fields and both
+    decay modes) on a ragged two-shard layout: bit for bit."""
+    rng = np.random.default_rng(900 + seed)
+    kw = _random_hparams(rng)
+    c = Case([(1, 200, 300), (2, 130, 129)], dp=2, seed=seed)
+    hp = fp8z.hparams(**kw)
+    mx = torch.zeros(c.cap * 512, dtype=torch.uint8, device="cuda")
+    for s in c.shards:
+        fp8z.fp8z_adamw_requant_step_mx(c.dev["p"], c.dev["g"], c.dev["m"], c.dev["v"], c.w_fp8, mx,
+                                        int(s["blk_begin"]), int(s["blk_count_real"]), hp,
+                                        desc=c.desc_dev, dev_status=c.status)
+    torch.cuda.synchronize()
+    assert c.status.item() == 0
+    p, g, m, v = (c.host[k].copy() for k in "pgmv")
+    q = np.zeros(c.cap * BLK, np.uint8)
+    sc = np.zeros(c.cap * 512, np.uint8)
+    oracle.adamw_requant_step_mx(p, g, m, v, q, sc, 0, int(c.summary["total_blocks"]),
+                                 oracle.Hparams.make(**kw),
+                                 desc=np.ascontiguousarray(c.blocks).view(oracle.BLOCK_DESC))
+    for k, want in (("p", p), ("m", m), ("v", v)):
+        assert np.array_equal(c.dev[k].cpu().numpy().view(np.uint32), want.view(np.uint32)), k
+    assert np.array_equal(c.w_fp8.cpu().numpy(), q)
+    data = np.repeat(c.blocks["param"] >= 0, 512)
+    assert np.array_equal(mx.cpu().numpy()[data], sc[data])
