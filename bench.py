@@ -655,11 +655,17 @@ def cpu_baseline(w, hp_kw, args, threads=None):
     nblocks = args.cpu_blocks
     host = sample_host_blocks(w, nblocks)
     secs = cpu_oracle_run(w, host, {**hp_kw, "step": int(hp_kw["step"])}, threads)
+    # the same oracle on one core, on the first 1/16 of the sample
+    n1 = max(1, nblocks // 16)
+    one = {k: v[:n1 * BLK].copy() for k, v in host.items()}
+    secs1 = cpu_oracle_run(w, one, {**hp_kw, "step": int(hp_kw["step"])}, 1)
     return {"value": round(nblocks * BLK / secs / 1e9, 6), "unit": UNIT, "cores": threads,
             "kind": "oracle",
             "sample": f"{nblocks} full 128x128 blocks ({nblocks * BLK} elements) of the {w.name} "
                       f"distributions, one oracle step, {threads} threads over block ranges, "
-                      f"{secs:.2f} s wall"}
+                      f"{secs:.2f} s wall",
+            "single_core": {"value": round(n1 * BLK / secs1 / 1e9, 6), "unit": UNIT,
+                            "sample": f"{n1} blocks, {secs1:.2f} s wall"}}
 
 
 def run_reference(args):
