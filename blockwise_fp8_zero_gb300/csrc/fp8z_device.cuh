@@ -91,6 +91,17 @@ __device__ __forceinline__ uint64_t l2_evict_first_policy() {
     return pol;
 }
 
+__device__ __forceinline__ uint64_t l2_evict_last_policy() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// 4-byte global store carrying an L2 eviction policy.
+__device__ __forceinline__ void store_u32_hint(void* dst, uint32_t x, uint64_t pol) {
+    asm volatile("st.global.L2::cache_hint.b32 [%0], %1, %2;" ::"l"(dst), "r"(x), "l"(pol) : "memory");
+}
+
 // Global -> shared bulk copy on the TMA engine; completion is counted as
 // transaction bytes on `bar`.  dst, src 16-byte aligned, bytes % 16 == 0.
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,

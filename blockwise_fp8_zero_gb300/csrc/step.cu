@@ -307,19 +307,21 @@ __device__ __forceinline__ bool dest_ok(const StepArgs& A, const BlockInfo& bi, 
 // Row-major E4M3 write of one block into the whole-param buffer ("Summary"
 // of the ZeRO design page: the FP8 params are unfolded back to their 2-D/3-D
 // shape; here the unfold happens on the way out).  Row r of the block is 128
-// contiguous bytes of row brow*128 + r of the param.
+// contiguous bytes of row brow*128 + r of the param; like the column-major
+// copy's, these scattered rows are stored with the L2 evict-last policy.
 __device__ __forceinline__ void store_rowmajor(const StepArgs& A, const BlockInfo& bi, const ParamInfo& pi,
                                                const uint32_t (&words)[kKeep], int warp, int col) {
     const int64_t H = pi.H, W = pi.W;
     const int64_t base = pi.t_off + bi.e * H * W + int64_t(bi.brow) * kBlk * W + int64_t(bi.bcol) * kBlk;
     const bool aligned = ((pi.t_off + bi.e * H * W) | W) % 4 == 0;
+    const uint64_t keep_in_l2 = l2_evict_last_policy();
 #pragma unroll
     for (int k = 0; k < kKeep; ++k) {
         const int row = k * kConsumerWarps + warp;
         if (row >= bi.vr || col >= bi.vc) continue;
         uint8_t* dst = A.w_row + base + int64_t(row) * W + col;
         if (aligned && col + 3 < bi.vc) {
-            store_word(dst, words[k]);
+            store_u32_hint(dst, words[k], keep_in_l2);
         } else {
             for (int b = 0; b < 4 && col + b < bi.vc; ++b) dst[b] = uint8_t(words[k] >> (8 * b));
         }
@@ -328,7 +330,11 @@ __device__ __forceinline__ void store_rowmajor(const StepArgs& A, const BlockInf
 
 // Column-major copy of one block: the quantized words go through a swizzled
 // shared tile; each warp then writes four output rows per pass, 128
-// contiguous bytes per warp store.  column_major_in stages the block (false
+// contiguous bytes per warp store.  The stores carry an L2 evict-last policy:
+// a block adds 128 bytes to each of 128 output rows, and lines kept longer in
+// L2 meet their row neighbours from other blocks before they are written back
+// (28.24 -> 27.93 ms per step on GB300 at 117 x 7168^2; 1.0 of the lines beat
+// 0.5 and 0.25).  column_major_in stages the block (false
 // when the descriptor does not match the param table: nothing is staged);
 // column_major_out waits until every warp has staged its rows and writes the
 // block out (false when that wait gave up).
@@ -356,6 +362,7 @@ __device__ __forceinline__ bool column_major_out(const StepArgs& A, const BlockI
                                                  int lane) {
     if (!mbar_wait_bounded(tile_bar, tile_phase, wd)) return false;
     tile_phase ^= 1;
+    const uint64_t keep_in_l2 = l2_evict_last_policy();
     const int64_t H = pi.H;
     const int64_t t_base = pi.t_off + bi.e * H * pi.W;
     const bool aligned = ((t_base | H) & 3) == 0;
@@ -375,7 +382,7 @@ __device__ __forceinline__ bool column_major_out(const StepArgs& A, const BlockI
             if (c >= bi.vc || r0 >= bi.vr) continue;
             uint8_t* dst = out_blk + (bi.bcol * int64_t(kBlk) + c) * H + r0;
             if (aligned && r0 + 3 < bi.vr) {
-                store_word(dst, o[cc]);
+                store_u32_hint(dst, o[cc], keep_in_l2);
             } else {
                 for (int b = 0; b < 4 && r0 + b < bi.vr; ++b) dst[b] = uint8_t(o[cc] >> (8 * b));
             }
