@@ -137,6 +137,9 @@ template <bool kF16>
 __device__ __forceinline__ void transpose_tile_words(const uint32_t* tile, int warp, int r0, uint8_t* out,
                                                      int64_t R, uint32_t rr01, uint32_t rr23,
                                                      const float (&ratio)[4]) {
+    // The 128-byte pieces land in 128 output rows R bytes apart; keeping them
+    // in L2 until the rest of each row's sector arrives saves partial writes.
+    const uint64_t keep_in_l2 = l2_evict_last_policy();
 #pragma unroll
     for (int h = 0; h < 4; ++h) {
         const int cg = warp + 8 * h;                     // input columns 4cg..4cg+3
@@ -157,7 +160,7 @@ __device__ __forceinline__ void transpose_tile_words(const uint32_t* tile, int w
                 word = pack_e4m3x4(__fmul_rn(a.x, ratio[0]), __fmul_rn(a.y, ratio[1]),
                                    __fmul_rn(b.x, ratio[2]), __fmul_rn(b.y, ratio[3]));
             }
-            *reinterpret_cast<uint32_t*>(dst) = word;
+            store_u32_hint(dst, word, keep_in_l2);
             dst += R;
         }
     }
