@@ -13,8 +13,9 @@
 //
 // Traffic: quantize 4 B in + 1 B out per element, the transpose 1 B in + 1 B
 // out per element (+ 1/32 B of scales each way).  The quantizer runs at the
-// HBM bound; the transpose at the pace of its re-expression arithmetic (about
-// 31 instructions per 4-byte output word keep the ALU pipe near 56 %).
+// HBM bound; the transpose at the pace of its re-expression arithmetic and
+// the latency of its staging loads (about 26 instructions per 4-byte output
+// word, the ALU pipe near 52 %, DRAM near 75 %).
 #include <cfloat>
 #include <cstdint>
 
@@ -166,29 +167,30 @@ __device__ __forceinline__ void transpose_tile_words(const uint32_t* tile, int w
     }
 }
 
-// Re-express one staged 128x128 tile (row tile i, column tile j) under its
-// largest row scale and write it column-wise.  Lane l of every warp owns input
-// rows 4l..4l+3: it reads their four row scales, the warp reduces the tile's
-// largest scale s', and the lane keeps the four ratios s_r / s'.  Each warp
-// then writes four output rows (input columns) per pass, re-expressing the four
-// bytes of each output word with their rows' ratios (decode, multiply, one
-// rounding to E4M3; in f16x2 when the whole warp's ratios allow it), a warp
-// writing 128 contiguous bytes of one output row.
-__device__ __forceinline__ void transpose_tile_out(const uint32_t* tile, const float* scales, int64_t i,
-                                                   int64_t j, int64_t R, int64_t ntr, uint8_t* qt,
-                                                   float* st, int warp, int lane, bool write_st,
-                                                   int st_row) {
+// The ratios of one 128x128 tile (row tile i, column tile j), computed by one
+// warp: lane l reads the row scales of input rows 4l..4l+3, the warp reduces
+// the tile's largest scale s' (the column-wise scale of all 128 output rows,
+// which the warp writes), and the lane keeps the four ratios s_r / s' (IEEE
+// divide) in FP32 and as f16x2 pairs.  The f16x2 re-expression is chosen for
+// the tile when every ratio is a power of two 2^-D with D <= 15: an E4M3 value
+// times such a ratio has its lowest bit at or above 2^-24, so the product is
+// exact in FP16 and decode, multiply and one rounding run as f16x2.
+struct TileRatios {
+    float4 ratio[32];                     // lane l: rows 4l..4l+3
+    uint2 f16[32];                        // the same, as two f16x2 pairs
+    int use_f16;
+};
+
+__device__ __forceinline__ void tile_ratios(const float* s, int64_t i, int64_t j, int64_t ntc, int64_t ntr,
+                                            float* st, int lane, TileRatios& out) {
     const int r0 = lane * 4;
     float sr[4];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) sr[k] = scales[r0 + k];
+    for (int k = 0; k < 4; ++k) sr[k] = __ldg(s + (i * kTile + r0 + k) * ntc + j);
     float smax = fmaxf(fmaxf(sr[0], sr[1]), fmaxf(sr[2], sr[3]));
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) smax = fmaxf(smax, __shfl_xor_sync(0xFFFFFFFFu, smax, o));
     float ratio[4];
-    // Power-of-two ratios 2^-D with D <= 15: an E4M3 value times 2^-D has its
-    // lowest bit at or above 2^-24, so the product is exact in FP16 and the
-    // whole re-expression can run as f16x2 (decode, multiply, one rounding).
     bool pow2_small = true;
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
@@ -197,44 +199,47 @@ __device__ __forceinline__ void transpose_tile_out(const uint32_t* tile, const f
         const int d = 127 - int(rb >> 23);
         pow2_small = pow2_small && (rb & 0x7FFFFFu) == 0 && (rb >> 23) != 0 && d >= 0 && d <= 15;
     }
-    const bool warp_f16 = __all_sync(0xFFFFFFFFu, pow2_small);
-    const uint32_t rr01 = f16x2_pack(ratio[0], ratio[1]);
-    const uint32_t rr23 = f16x2_pack(ratio[2], ratio[3]);
-    if (write_st) st[(j * kTile + st_row) * ntr + i] = smax;
-    uint8_t* out = qt + (j * kTile) * R + i * kTile + r0;
-    if (warp_f16)
-        transpose_tile_words<true>(tile, warp, r0, out, R, rr01, rr23, ratio);
-    else
-        transpose_tile_words<false>(tile, warp, r0, out, R, rr01, rr23, ratio);
+    const bool use_f16 = __all_sync(0xFFFFFFFFu, pow2_small);
+    out.ratio[lane] = make_float4(ratio[0], ratio[1], ratio[2], ratio[3]);
+    out.f16[lane] = make_uint2(f16x2_pack(ratio[0], ratio[1]), f16x2_pack(ratio[2], ratio[3]));
+    if (lane == 0) out.use_f16 = use_f16;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) st[(j * kTile + r0 + k) * ntr + i] = smax;
 }
 
 // One CTA per strip of kW column tiles of one row tile: the strip's rows are
-// read as kW*128 contiguous bytes, staged in swizzled shared tiles with their
-// row scales, then each tile is written out column-wise by all eight warps.
-// Consecutive CTAs take consecutive row tiles of one strip, so their output
-// rows continue each other in memory.  Measured on GB300 at 65536x7168: 0.172
-// ms with two-tile strips, 0.189 ms with one tile per CTA (128-byte reads per
-// row), 0.201 ms with column tiles fastest; a persistent variant that moved the
-// tiles with TMA (128B-swizzled loads and stores) reached 0.181 ms: the
-// re-expression arithmetic, not the memory system, sets the pace.  The tile
-// loop stays rolled: unrolled, the two copies of both re-expression paths
-// ran at 0.218 ms.  Tiles are kTileWords apart, not 4096, so the two tiles'
-// row writes fall on different banks.
+// read as kW*128 contiguous bytes and staged in swizzled shared tiles while
+// warp u computes the ratios of tile u; then each tile is written out
+// column-wise by all eight warps, lane l re-expressing the bytes of input
+// rows 4l..4l+3 with their ratios, a warp writing 128 contiguous bytes of one
+// output row per store.  Consecutive CTAs take consecutive row tiles of one
+// strip, so their output rows continue each other in memory.  Measured on
+// GB300 at 65536x7168: 0.162 ms with three CTAs per SM (80 registers; 0.166
+// ms at 64 registers and four CTAs, 0.192 ms at 48 and five, 0.181 ms at 93
+// and two); 0.170 ms when all eight warps computed the
+// same ratios (four IEEE divides per lane per tile, a fifth of the
+// instructions); 0.166-0.189 ms with the ratio arithmetic after the staging
+// stores (the strided scale loads then sit on the CTA's critical path); 0.189
+// ms with one tile per CTA (128-byte reads per row), 0.201 ms with column
+// tiles fastest; a persistent variant that moved the tiles with TMA
+// (128B-swizzled loads and stores) reached 0.181 ms: the re-expression
+// arithmetic, not the memory system, sets the pace.  The tile loop stays
+// rolled: unrolled, the two copies of both re-expression paths ran 25 %
+// slower.  Tiles are kTileWords apart, not 4096, so the two tiles' row writes
+// fall on different banks.
 constexpr int kTileWords = kTile * kTile / 4 + 2;
 
 template <int kW>
-__global__ void __launch_bounds__(256) transpose_rowwise_kernel(const uint8_t* __restrict__ q,
+__global__ void __launch_bounds__(256, 3) transpose_rowwise_kernel(const uint8_t* __restrict__ q,
                                                                 const float* __restrict__ s,
                                                                 int64_t R, int64_t C,
                                                                 uint8_t* __restrict__ qt,
                                                                 float* __restrict__ st) {
     __shared__ uint32_t tile[kW][kTileWords];
-    __shared__ float scales[kW][kTile];
+    __shared__ TileRatios ratios[kW];
     const int64_t ntc = C / kTile, ntr = R / kTile;
     const int64_t i = blockIdx.x % ntr, jw = (blockIdx.x / ntr) * kW;   // first column tile of the strip
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    for (int x = tid; x < kW * kTile; x += 256)
-        scales[x / kTile][x % kTile] = __ldg(s + (i * kTile + x % kTile) * ntc + jw + x / kTile);
 
     // 16-byte chunks: row r of the strip is 8*kW chunks, chunk ch of tile ch/8
     constexpr int kChunks = kW * 8;
@@ -246,6 +251,7 @@ __global__ void __launch_bounds__(256) transpose_rowwise_kernel(const uint8_t* _
         const int idx = it * 256 + tid;
         buf[it] = __ldcs(src + (idx / kChunks) * (C / 16) + idx % kChunks);
     }
+    if (warp < kW) tile_ratios(s, i, jw + warp, ntc, ntr, st, lane, ratios[warp]);
 #pragma unroll
     for (int it = 0; it < kIters; ++it) {
         const int idx = it * 256 + tid;
@@ -258,9 +264,18 @@ __global__ void __launch_bounds__(256) transpose_rowwise_kernel(const uint8_t* _
         row[(w0 + 3) ^ sw] = buf[it].w;
     }
     __syncthreads();
+    const int r0 = lane * 4;
 #pragma unroll 1
-    for (int u = 0; u < kW; ++u)
-        transpose_tile_out(tile[u], scales[u], i, jw + u, R, ntr, qt, st, warp, lane, tid < kTile, tid);
+    for (int u = 0; u < kW; ++u) {
+        const float4 rt = ratios[u].ratio[lane];
+        const uint2 rr = ratios[u].f16[lane];
+        const float ratio[4] = {rt.x, rt.y, rt.z, rt.w};
+        uint8_t* out = qt + ((jw + u) * kTile) * R + i * kTile + r0;
+        if (ratios[u].use_f16)
+            transpose_tile_words<true>(tile[u], warp, r0, out, R, rr.x, rr.y, ratio);
+        else
+            transpose_tile_words<false>(tile[u], warp, r0, out, R, rr.x, rr.y, ratio);
+    }
 }
 
 }  // namespace
