@@ -222,8 +222,10 @@ __device__ __forceinline__ void tile_ratios(const float* s, int64_t i, int64_t j
 // stores (the strided scale loads then sit on the CTA's critical path); 0.189
 // ms with one tile per CTA (128-byte reads per row), 0.201 ms with column
 // tiles fastest; a persistent variant that moved the tiles with TMA
-// (128B-swizzled loads and stores) reached 0.181 ms: the re-expression
-// arithmetic, not the memory system, sets the pace.  The tile loop stays
+// (128B-swizzled loads and stores) reached 0.181 ms, and one that prefetched
+// the next strip into registers while writing the current one 0.175-0.196 ms
+// (two to four CTAs per SM): the re-expression arithmetic, not the memory
+// system, sets the pace.  The tile loop stays
 // rolled: unrolled, the two copies of both re-expression paths ran 25 %
 // slower.  Tiles are kTileWords apart, not 4096, so the two tiles' row writes
 // fall on different banks.
