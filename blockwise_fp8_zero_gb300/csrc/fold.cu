@@ -14,7 +14,9 @@
 // TMA engine: fold = one tiled tensor-map load of the tile (the engine fills the
 // ragged edge with zeros) + one bulk store of the contiguous block; unfold =
 // one bulk load + one tiled tensor-map store (the engine clips at the tensor's
-// edge).  Persistent CTAs keep 192 KB of blocks in flight per SM.  Shapes
+// edge).  Persistent CTAs keep rings of blocks in flight (FP32: one CTA per
+// SM, 192 KB; bytes: two CTAs per SM, 80 KB each, one store in flight beside
+// the loads).  Shapes
 // whose row pitch is not a multiple of 16 bytes (a TMA rule) take a plain
 // kernel instead.
 #include <cstdint>
@@ -53,22 +55,29 @@ __device__ __forceinline__ void tile_coords(const FoldArgs& F, int64_t b, int& x
 }
 
 // One thread per CTA drives the copies.  Blocks are dealt round-robin over a
-// persistent grid; each CTA keeps a ring of block buffers, all but one holding
-// loads in flight while the oldest is written out.  FP32 blocks (64 KB): one
-// CTA per SM with a 192 KB ring; byte blocks (16 KB): three CTAs per SM with
-// 64 KB rings, so three threads issue per SM (E4M3 unfold 0.95 of the copy
-// bandwidth on GB300 against 0.925 with one CTA and a 192 KB ring).
+// persistent grid; each CTA keeps a ring of nbuf block buffers: kLag of them
+// may still be read by their stores while nbuf - 1 - kLag hold loads in flight
+// and one is being written out.  FP32 blocks (64 KB): one CTA per SM with a
+// 192 KB ring (3 buffers, no store slack); byte blocks (16 KB): two CTAs per
+// SM with 80 KB rings, three loads ahead and one store in flight.  Measured on
+// GB300, fractions of the copy bandwidth, E4M3 unfold / fold: at 32 x 7168^2
+// 0.963 / 0.959 against 0.946 / 0.947 for three CTAs with 64 KB rings and no
+// slack (two loads ahead 0.940, four 0.945; one CTA with a 192 KB ring
+// 0.925); at 117 x 7168^2 every one of these runs the unfold at 0.941 and the
+// fold at 0.945-0.950.
 constexpr int kRingBytesF32 = 192 * 1024;
-constexpr int kRingBytesU8 = 64 * 1024;
-constexpr int kCtasPerSmU8 = 3;
+constexpr int kStoreLagF32 = 0;
+constexpr int kRingBytesU8 = 80 * 1024;
+constexpr int kCtasPerSmU8 = 2;
+constexpr int kStoreLagU8 = 1;
 
-template <bool kFold>
+template <bool kFold, int kLag>
 __global__ void __launch_bounds__(32) fold_tma_kernel(const __grid_constant__ CUtensorMap map,
                                                       const FoldArgs F) {
     extern __shared__ __align__(1024) unsigned char smem[];
     if (threadIdx.x != 0) return;
     const uint32_t box = uint32_t(kBlkElems) * F.esz;
-    const int nbuf = F.nbuf;                              // 3 (fp32) or 4 (bytes)
+    const int nbuf = F.nbuf;                              // 3 (fp32) or 5 (bytes)
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + size_t(nbuf) * box);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + nbuf);
     const uint32_t buf0 = smem_addr(smem);
@@ -93,12 +102,14 @@ __global__ void __launch_bounds__(32) fold_tma_kernel(const __grid_constant__ CU
         }
     };
 
-    const int64_t ahead = nbuf - 1;
+    const int64_t ahead = nbuf - 1 - kLag;                // >= 1 (host checks)
     for (int64_t i = 0; i < count && i < ahead; ++i) issue_load(i);
     for (int64_t i = 0; i < count; ++i) {
         const int64_t j = i + ahead;
         if (j < count) {
-            bulk_wait_read<0>();     // block i-1's store has read its buffer (= buffer of block j)
+            // block j reuses the buffer of block i-1-kLag: at most the kLag
+            // newest store groups (blocks i-kLag..i-1) may still be reading
+            bulk_wait_read<kLag>();
             issue_load(j);
         }
         const int s = int(i % nbuf);
@@ -184,20 +195,29 @@ int run(bool fold, const void* src, int32_t esz, const fp8z_param_entry* entry, 
                                 CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
                                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         if (cr == CUDA_SUCCESS) {
-            const int ring = esz == 4 ? kRingBytesF32 : kRingBytesU8;
+            const bool f32 = esz == 4;
+            const int ring = f32 ? kRingBytesF32 : kRingBytesU8;
             const int nbuf = ring / (kBlkElems * esz);
+            static_assert(kRingBytesF32 / (kBlkElems * 4) - 1 - kStoreLagF32 >= 1, "FP32 ring too small");
+            static_assert(kRingBytesU8 / kBlkElems - 1 - kStoreLagU8 >= 1, "byte ring too small");
             FoldArgs F{flat, pe.hb, pe.wb, nblk, esz, nbuf, dev_status, host::kDefaultTimeoutNs};
             const int smem = ring + nbuf * 8 + 16;
-            const void* k = fold ? reinterpret_cast<const void*>(&fold_tma_kernel<true>)
-                                 : reinterpret_cast<const void*>(&fold_tma_kernel<false>);
-            rc = host::set_smem_once(k, fold ? 2 : 3, smem);
+            const void* k = fold ? (f32 ? reinterpret_cast<const void*>(&fold_tma_kernel<true, kStoreLagF32>)
+                                        : reinterpret_cast<const void*>(&fold_tma_kernel<true, kStoreLagU8>))
+                                 : (f32 ? reinterpret_cast<const void*>(&fold_tma_kernel<false, kStoreLagF32>)
+                                        : reinterpret_cast<const void*>(&fold_tma_kernel<false, kStoreLagU8>));
+            rc = host::set_smem_once(k, fold ? (f32 ? 2 : 7) : (f32 ? 3 : 8), smem);
             if (rc != FP8Z_OK) return rc;
-            const int64_t cap = int64_t(sms) * (esz == 4 ? 1 : kCtasPerSmU8);
+            const int64_t cap = int64_t(sms) * (f32 ? 1 : kCtasPerSmU8);
             const unsigned grid = unsigned(nblk < cap ? nblk : cap);
-            if (fold)
-                fold_tma_kernel<true><<<grid, 32, smem, st>>>(map, F);
+            if (fold && f32)
+                fold_tma_kernel<true, kStoreLagF32><<<grid, 32, smem, st>>>(map, F);
+            else if (fold)
+                fold_tma_kernel<true, kStoreLagU8><<<grid, 32, smem, st>>>(map, F);
+            else if (f32)
+                fold_tma_kernel<false, kStoreLagF32><<<grid, 32, smem, st>>>(map, F);
             else
-                fold_tma_kernel<false><<<grid, 32, smem, st>>>(map, F);
+                fold_tma_kernel<false, kStoreLagU8><<<grid, 32, smem, st>>>(map, F);
             return cudaGetLastError() == cudaSuccess ? FP8Z_OK : FP8Z_ECUDA;
         }
     }

@@ -71,7 +71,7 @@ int device_sms(int* sms) {
 
 namespace {
 constexpr int kMaxDevices = 64;
-constexpr int kMaxSlots = 8;
+constexpr int kMaxSlots = 10;
 std::atomic<int> g_smem_done[kMaxSlots][kMaxDevices];
 }  // namespace
 
