@@ -1,7 +1,8 @@
 """Full-size workloads on the GPU, checked against the oracle on sampled
 blocks (blocks are independent, so a block computed alone by the oracle is
-the exact expected value): every ragged edge block, the first and last block
-of every shard, and a seeded random sample.  Same bit-exact bar as the small
+the exact expected value): every ragged edge block (14,635 in the 500-matrix
+workload), the first and last block of every shard, and a seeded random
+sample of 1500.  Same bit-exact bar as the small
 cases.  The 6e9-element workload runs in the launch configuration the
 benchmark times (one launch over all blocks, column-major copy on)."""
 import numpy as np
@@ -15,6 +16,7 @@ from _gpu_util import assert_bitexact, oracle_blocks  # noqa: E402
 
 pytestmark = pytest.mark.gpu
 BLK = fp8z.BLOCK_ELEMS
+CHUNK = 2048
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -28,13 +30,11 @@ def _lib():
     torch.cuda.empty_cache()
 
 
-def _sample(blocks, shards, n_random=1500, max_ragged=2000, seed=0):
+def _sample(blocks, shards, n_random=1500, seed=0):
     data = np.nonzero(blocks["param"] >= 0)[0]
     rng = np.random.default_rng(seed)
     pick = set(rng.choice(data, size=min(n_random, data.size), replace=False).tolist())
     ragged = np.nonzero((blocks["param"] >= 0) & ((blocks["valid_rows"] < 128) | (blocks["valid_cols"] < 128)))[0]
-    if ragged.size > max_ragged:
-        ragged = rng.choice(ragged, size=max_ragged, replace=False)
     pick |= set(ragged.tolist())
     for s in shards:
         if s["blk_count_real"] > 0:
@@ -76,12 +76,21 @@ def run_sampled(oracle, w, one_launch=False):
                                      w_fp8_t=wt, inv_scale_t=it, dev_status=st)
     torch.cuda.synchronize()
     assert st.item() == 0, fp8z.fp8z_status_string(st.item())
-    got = {k: _gather(state[k], idx, BLK) for k in "pmv"}
-    got["q"] = _gather(q, idx, BLK)
-    got["inv"] = inv[torch.from_numpy(idx).to(dev)].cpu().numpy()
-    d = np.ascontiguousarray(blocks[idx]).view(oracle.BLOCK_DESC)
-    qo, invo = oracle_blocks(oracle, hp, pre["p"], pre["g"], pre["m"], pre["v"], d)
-    assert_bitexact(got, dict(p=pre["p"], m=pre["m"], v=pre["v"], q=qo, inv=invo))
+    # checked in chunks of blocks, so the host holds the inputs of the sample
+    # (gathered before the step) and one chunk of outputs at a time
+    for c0 in range(0, idx.size, CHUNK):
+        ii = idx[c0:c0 + CHUNK]
+        got = {k: _gather(state[k], ii, BLK) for k in "pmv"}
+        got["q"] = _gather(q, ii, BLK)
+        got["inv"] = inv[torch.from_numpy(ii).to(dev)].cpu().numpy()
+        d = np.ascontiguousarray(blocks[ii]).view(oracle.BLOCK_DESC)
+        sl = slice(c0 * BLK, (c0 + ii.size) * BLK)
+        pc = {k: pre[k][sl] for k in "pgmv"}
+        qc, invc = oracle_blocks(oracle, hp, pc["p"], pc["g"], pc["m"], pc["v"], d)
+        assert_bitexact(got, dict(p=pc["p"], m=pc["m"], v=pc["v"], q=qc, inv=invc))
+        if c0 == 0:
+            qo, invo = qc, invc
+        del got
     if w.transposed:
         # the column-major copy of each sampled block is its oracle tile, transposed
         for j, b in enumerate(idx[:400]):
