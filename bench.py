@@ -630,7 +630,12 @@ def run_e2e(args, w, state, q, inv, wt, it, desc, pdev, params, shards, hp_kw, t
                     it_host[s0:s0 + nb].copy_(it[s0:s0 + nb], non_blocking=True)
                 e_out.record(s_out)
             sent[u] = e_out
+        # end of this step's work: its last output copy
+        done = torch.cuda.Event(enable_timing=True)
+        done.record(s_out)
+        step_done.append(done)
 
+    step_done = []
     one(t)
     torch.cuda.synchronize(dev)
     t0 = time.perf_counter()
@@ -639,8 +644,14 @@ def run_e2e(args, w, state, q, inv, wt, it, desc, pdev, params, shards, hp_kw, t
     torch.cuda.synchronize(dev)
     secs = max_over_ranks(time.perf_counter() - t0, dev)
     real = sum(u[3] for u in units)
+    # time between the ends of consecutive steps (the steps overlap, so this is
+    # each step's share of the stream, not its latency)
+    step_ms = [step_done[i].elapsed_time(step_done[i + 1]) for i in range(len(step_done) - 1)]
+    med_ms = float(np.median(step_ms))
     return {"value": round(real * steps * ws / secs / 1e9, 4), "unit": UNIT,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
+            "step_ms": [round(x, 1) for x in step_ms],
+            "median_step_gelem_s": round(real * ws / (med_ms / 1e3) / 1e9, 4),
             "link": {"h2d_gbs": round(h2d_gbs, 1), "d2h_gbs": round(d2h_gbs, 1),
                      "both_gbs": round(both_gbs, 1),
                      "bound_gelem_s": round(real * ws / bound_s / 1e9, 2),
