@@ -1,6 +1,7 @@
 """The benchmark's JSON line on a one-tile case of the 6e9 workload: one
 line, every key the line promises, consistent numbers (value = elements /
-time, the roofline fraction = achieved / peak, one launch per timed step)."""
+time, the roofline fraction = achieved / peak, one launch per timed step,
+the end-to-end bytes per step of one 7168^2 tile)."""
 import json
 import os
 import subprocess
@@ -18,7 +19,7 @@ def test_bench_line_schema():
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     cmd = [sys.executable, os.path.join(ROOT, "bench.py"), "--workload", "flat6e9",
-           "--max-elems", str(7168 * 7168), "--steps", "4", "--warmup", "3", "--no-e2e",
+           "--max-elems", str(7168 * 7168), "--steps", "4", "--warmup", "3",
            "--no-cpu-baseline", "--no-aux"]
     out = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=600)
     assert out.returncode == 0, out.stderr[-2000:]
@@ -39,3 +40,11 @@ def test_bench_line_schema():
     assert abs(d["value"] - d["config"]["elements"] / (d["ms_per_step"] / 1e3) / 1e9) < 0.01 * d["value"]
     assert d["gpu_launches"] == d["steps"]
     assert {"sm_mhz", "sm_max_mhz", "reasons"} <= set(d["clocks"])
+    e = d["e2e"]
+    n = 7168 * 7168
+    assert e["unit"] == "Gelem/s" and e["value"] > 0 and e["median_step_gelem_s"] > 0
+    # grads in; codes + inverse scales + the column-major copy and its grid out
+    assert e["h2d_bytes_per_step"] == 4 * n
+    assert e["d2h_bytes_per_step"] == 2 * n + 2 * 4 * (n // 16384)
+    assert len(e["step_ms"]) == e["steps"] and all(x > 0 for x in e["step_ms"])
+    assert {"h2d_gbs", "d2h_gbs", "both_gbs", "bound_gelem_s"} <= set(e["link"])
