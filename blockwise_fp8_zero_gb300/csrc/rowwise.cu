@@ -14,8 +14,8 @@
 // Traffic: quantize 4 B in + 1 B out per element, the transpose 1 B in + 1 B
 // out per element (+ 1/32 B of scales each way).  The quantizer runs at the
 // HBM bound; the transpose at the pace of its re-expression arithmetic and
-// the latency of its staging loads (about 26 instructions per 4-byte output
-// word, the ALU pipe near 52 %, DRAM near 75 %).
+// the latency of its staging loads (about 24 instructions per 4-byte output
+// word, the ALU pipe near 44 %, DRAM near 76 %).
 #include <cfloat>
 #include <cstdint>
 
@@ -119,21 +119,47 @@ __device__ __forceinline__ uint32_t f16x2_pack(float lo, float hi) {
     return r;
 }
 
-// Two E4M3 codes (low byte first) times two FP16 factors, rounded once back
-// to E4M3 (nearest even, saturating).
-__device__ __forceinline__ uint32_t e4m3x2_scale_f16(uint32_t two_codes, uint32_t f16x2) {
-    uint32_t h;
-    uint16_t in = static_cast<uint16_t>(two_codes), out;
-    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"(in));
-    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(h) : "r"(h), "r"(f16x2));
-    asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(out) : "r"(h));
-    return out;
+// Re-express the bytes of two output words.  pair01 holds the codes of input
+// rows 0, 1 of column c (low half) and of column c+1 (high half), pair23 the
+// same for rows 2, 3; out_c / out_c1 get the four re-expressed codes of
+// columns c and c+1, row 0 in the low byte.  f16x2 path: decode two codes to
+// f16x2, multiply by the rows' two ratios, round once to E4M3 (nearest even,
+// saturating).
+__device__ __forceinline__ void rescale_words_f16(uint32_t pair01, uint32_t pair23, uint32_t rr01,
+                                                  uint32_t rr23, uint32_t& out_c, uint32_t& out_c1) {
+    asm("{\n\t.reg .b16 a0, a1, b0, b1, o0, o1, o2, o3;\n\t.reg .b32 h;\n\t"
+        "mov.b32 {a0, a1}, %2;\n\t"
+        "mov.b32 {b0, b1}, %3;\n\t"
+        "cvt.rn.f16x2.e4m3x2 h, a0;\n\tmul.rn.f16x2 h, h, %4;\n\tcvt.rn.satfinite.e4m3x2.f16x2 o0, h;\n\t"
+        "cvt.rn.f16x2.e4m3x2 h, b0;\n\tmul.rn.f16x2 h, h, %5;\n\tcvt.rn.satfinite.e4m3x2.f16x2 o1, h;\n\t"
+        "cvt.rn.f16x2.e4m3x2 h, a1;\n\tmul.rn.f16x2 h, h, %4;\n\tcvt.rn.satfinite.e4m3x2.f16x2 o2, h;\n\t"
+        "cvt.rn.f16x2.e4m3x2 h, b1;\n\tmul.rn.f16x2 h, h, %5;\n\tcvt.rn.satfinite.e4m3x2.f16x2 o3, h;\n\t"
+        "mov.b32 %0, {o0, o1};\n\t"
+        "mov.b32 %1, {o2, o3};\n\t}"
+        : "=r"(out_c), "=r"(out_c1)
+        : "r"(pair01), "r"(pair23), "r"(rr01), "r"(rr23));
+}
+
+// The same in FP32: decode, multiply by the row's ratio, round once to E4M3.
+__device__ __forceinline__ void rescale_words_f32(uint32_t pair01, uint32_t pair23, const float (&ratio)[4],
+                                                  uint32_t& out_c, uint32_t& out_c1) {
+    const float2 a0 = e4m3x2_to_float2(pair01), b0 = e4m3x2_to_float2(pair23);
+    const float2 a1 = e4m3x2_to_float2(pair01 >> 16), b1 = e4m3x2_to_float2(pair23 >> 16);
+    out_c = pack_e4m3x4(__fmul_rn(a0.x, ratio[0]), __fmul_rn(a0.y, ratio[1]), __fmul_rn(b0.x, ratio[2]),
+                        __fmul_rn(b0.y, ratio[3]));
+    out_c1 = pack_e4m3x4(__fmul_rn(a1.x, ratio[0]), __fmul_rn(a1.y, ratio[1]), __fmul_rn(b1.x, ratio[2]),
+                         __fmul_rn(b1.y, ratio[3]));
 }
 
 // The 128 output words of one warp pass set: input columns 4cg..4cg+3
 // (cg = warp + 8h) of rows r0..r0+3, read from the swizzled tile, 4x4
 // byte-transposed, re-expressed and written to output rows 4cg..4cg+3.  The
-// f16x2 / FP32 choice is made once per tile, outside these loops.
+// transpose stops after its first byte-permutation stage: each 16-bit half of
+// its words is already the pair of codes (rows r0, r0+1 or r0+2, r0+3 of one
+// column) that one conversion takes, so the re-expression reads them there and
+// its packing of the results is the second stage (0.1589 against 0.1617 ms
+// with the full transpose first, at 65536x7168).  The f16x2 / FP32 choice is
+// made once per tile, outside these loops.
 template <bool kF16>
 __device__ __forceinline__ void transpose_tile_words(const uint32_t* tile, int warp, int r0, uint8_t* out,
                                                      int64_t R, uint32_t rr01, uint32_t rr23,
@@ -147,21 +173,23 @@ __device__ __forceinline__ void transpose_tile_words(const uint32_t* tile, int w
         uint32_t w4[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) w4[k] = tile[(r0 + k) * 32 + (cg ^ tile_swz(r0 + k))];
-        uint32_t o[4];
-        transpose4x4(w4[0], w4[1], w4[2], w4[3], o[0], o[1], o[2], o[3]);
+        // rows r0, r0+1 (r0+2, r0+3) of columns 0|1 and of columns 2|3
+        const uint32_t p01_c01 = __byte_perm(w4[0], w4[1], 0x5140);
+        const uint32_t p01_c23 = __byte_perm(w4[0], w4[1], 0x7362);
+        const uint32_t p23_c01 = __byte_perm(w4[2], w4[3], 0x5140);
+        const uint32_t p23_c23 = __byte_perm(w4[2], w4[3], 0x7362);
+        uint32_t o[4];                                   // o[cc]: rows r0..r0+3 of column 4cg+cc
+        if (kF16) {
+            rescale_words_f16(p01_c01, p23_c01, rr01, rr23, o[0], o[1]);
+            rescale_words_f16(p01_c23, p23_c23, rr01, rr23, o[2], o[3]);
+        } else {
+            rescale_words_f32(p01_c01, p23_c01, ratio, o[0], o[1]);
+            rescale_words_f32(p01_c23, p23_c23, ratio, o[2], o[3]);
+        }
         uint8_t* dst = out + int64_t(4 * cg) * R;
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc) {
-            uint32_t word = o[cc];                       // bytes: rows r0..r0+3 of column 4cg+cc
-            if (kF16) {
-                word = e4m3x2_scale_f16(word, rr01) | (e4m3x2_scale_f16(word >> 16, rr23) << 16);
-            } else {
-                const float2 a = e4m3x2_to_float2(word);
-                const float2 b = e4m3x2_to_float2(word >> 16);
-                word = pack_e4m3x4(__fmul_rn(a.x, ratio[0]), __fmul_rn(a.y, ratio[1]),
-                                   __fmul_rn(b.x, ratio[2]), __fmul_rn(b.y, ratio[3]));
-            }
-            store_u32_hint(dst, word, keep_in_l2);
+            store_u32_hint(dst, o[cc], keep_in_l2);
             dst += R;
         }
     }
@@ -214,18 +242,20 @@ __device__ __forceinline__ void tile_ratios(const float* s, int64_t i, int64_t j
 // rows 4l..4l+3 with their ratios, a warp writing 128 contiguous bytes of one
 // output row per store.  Consecutive CTAs take consecutive row tiles of one
 // strip, so their output rows continue each other in memory.  Measured on
-// GB300 at 65536x7168: 0.162 ms with three CTAs per SM (80 registers; 0.166
-// ms at 64 registers and four CTAs, 0.192 ms at 48 and five, 0.181 ms at 93
-// and two); 0.170 ms when all eight warps computed the
-// same ratios (four IEEE divides per lane per tile, a fifth of the
-// instructions); 0.166-0.189 ms with the ratio arithmetic after the staging
+// GB300 at 65536x7168: 0.159 ms with three CTAs per SM (80 registers; 0.162
+// ms at 64 registers and four CTAs, 0.175 ms at 93 and two; before the
+// one-stage transpose, 0.192 ms at 48 registers and five); before that,
+// 0.170 against 0.162 ms when all eight warps computed the same ratios (four
+// IEEE divides per lane per tile, a fifth of the instructions); 0.166-0.189
+// ms with the ratio arithmetic after the staging
 // stores (the strided scale loads then sit on the CTA's critical path); 0.189
 // ms with one tile per CTA (128-byte reads per row), 0.201 ms with column
 // tiles fastest; a persistent variant that moved the tiles with TMA
 // (128B-swizzled loads and stores) reached 0.181 ms, and one that prefetched
 // the next strip into registers while writing the current one 0.175-0.196 ms
-// (two to four CTAs per SM): the re-expression arithmetic, not the memory
-// system, sets the pace.  The tile loop stays
+// (two to four CTAs per SM): the re-expression arithmetic and the staging
+// loads' latency, not the memory system's bandwidth, set the pace.  The tile
+// loop stays
 // rolled: unrolled, the two copies of both re-expression paths ran 25 %
 // slower.  Tiles are kTileWords apart, not 4096, so the two tiles' row writes
 // fall on different banks.
