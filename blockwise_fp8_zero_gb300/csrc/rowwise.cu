@@ -253,7 +253,9 @@ __device__ __forceinline__ void tile_ratios(const float* s, int64_t i, int64_t j
 // tiles fastest; a persistent variant that moved the tiles with TMA
 // (128B-swizzled loads and stores) reached 0.181 ms, and one that prefetched
 // the next strip into registers while writing the current one 0.175-0.196 ms
-// (two to four CTAs per SM): the re-expression arithmetic and the staging
+// (two to four CTAs per SM), and one that staged the output words in plain
+// shared tiles written by one 2-D TMA tensor store each 0.20-0.26 ms: the
+// re-expression arithmetic and the staging
 // loads' latency, not the memory system's bandwidth, set the pace.  The tile
 // loop stays
 // rolled: unrolled, the two copies of both re-expression paths ran 25 %
