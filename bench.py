@@ -528,8 +528,63 @@ def time_aux_kernels(w, q, inv, params, dev, stream, peak, reps=5, g=None, fused
               "fp8z_quantize_rowwise")
     timed_act(lambda: fp8z.fp8z_transpose_rowwise(qa, sa, qta, sta, stream=stream), 2 * n + 8 * n // 128,
               "fp8z_transpose_rowwise")
-    del xa, qa, sa, qta, sta
+    del qa, sa, qta, sta
+    try:
+        out["rowwise_double_quantization"] = rowwise_error_study(xa, stream)
+    except RuntimeError:
+        pass
+    del xa
     return out
+
+
+def rowwise_error_study(x, stream):
+    """The double-quantization error ("FP8-Flow-MoE" §3.1) at the bench's
+    activation size: X quantized row-wise (1x128 tiles) by the library, then
+    brought to the column-wise layout three ways -- the library's
+    scaling-aware transpose; the naive path (dequantize, transpose, quantize
+    column-wise again, the quantize being the library's); and quantizing X^T
+    directly -- each compared with X^T.  Torch ops only decode codes and sum
+    errors here (measurement, not the path).  Reported per scale rule:
+    sum|v - X^T| / sum|X^T| for each layout, and the fraction of values that
+    differ from the row-layout values (re-rounded or underflowed)."""
+    import torch
+    from blockwise_fp8_zero_gb300 import fp8z
+    T, Hd = x.shape
+
+    def decode(q, s):
+        return q.view(torch.float8_e4m3fn).float() * s.repeat_interleave(128, dim=1)
+
+    def quant(v, pow2):
+        q = torch.empty(v.shape, dtype=torch.uint8, device=v.device)
+        sc = torch.empty(v.shape[0], v.shape[1] // 128, device=v.device)
+        fp8z.fp8z_quantize_rowwise(v, pow2, q, sc, stream=stream)
+        return q, sc
+
+    res = {}
+    with torch.cuda.stream(stream):
+        xt = x.t().contiguous()
+        denom = xt.abs().double().sum()
+        rel = lambda v: float((v.double() - xt.double()).abs().sum() / denom)
+        for name, pow2 in (("pow2_scales", True), ("amax448_scales", False)):
+            q, sc = quant(x, pow2)
+            v_row_t = decode(q, sc).t().contiguous()        # the row-layout values, transposed
+            qt = torch.empty(Hd, T, dtype=torch.uint8, device=x.device)
+            st = torch.empty(Hd, T // 128, device=x.device)
+            fp8z.fp8z_transpose_rowwise(q, sc, qt, st, stream=stream)
+            v_sa = decode(qt, st)
+            del q, sc, qt, st
+            v_naive = decode(*quant(v_row_t, pow2))
+            v_direct = decode(*quant(xt, pow2))
+            res[name] = {"err_scaling_aware": round(rel(v_sa), 6), "err_naive": round(rel(v_naive), 6),
+                         "err_direct": round(rel(v_direct), 6),
+                         "changed_scaling_aware": round(float((v_sa != v_row_t).double().mean()), 6),
+                         "changed_naive": round(float((v_naive != v_row_t).double().mean()), 6)}
+            del v_row_t, v_sa, v_naive, v_direct
+    torch.cuda.synchronize()
+    res["param"] = f"{T}x{Hd} activation"
+    res["note"] = ("err_* = sum|v - X^T| / sum|X^T|; changed_* = fraction of values that differ "
+                   "from the row-layout values")
+    return res
 
 
 def run_e2e(args, w, state, q, inv, wt, it, desc, pdev, params, shards, hp_kw, t, dev, ws):
