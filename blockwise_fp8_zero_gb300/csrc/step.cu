@@ -535,6 +535,11 @@ __global__ void __launch_bounds__(kThreads, 1) fp8z_step_kernel(const StepArgs A
                 m4[r] = lds4(st + 2 * kStageElems + e0);
                 v4[r] = lds4(st + 3 * kStageElems + e0);
             }
+            // The slot is refilled by the TMA engine (async proxy) once every warp
+            // has arrived; the proxy fence orders this thread's generic reads of
+            // it before that write.  Without it a variant that kept the loaded
+            // values unused for a stage read refilled data in some runs.
+            fence_proxy_async();
             __syncwarp();
             if (lane == 0) mbar_arrive(empty0 + 8 * slot);
             if (++slot == kRing) { slot = 0; phase ^= 1; }
