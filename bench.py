@@ -283,6 +283,7 @@ def run_ours(args):
     with ClockSampler(uuid) as clocks:
         barrier()
         torch.cuda.synchronize(dev)
+        torch.cuda.nvtx.range_push("timed_steps")
         with torch.cuda.stream(stream):
             ev[0].record(stream)
             for i in range(args.steps):
@@ -290,6 +291,7 @@ def run_ours(args):
                 t += 1
                 ev[i + 1].record(stream)
         torch.cuda.synchronize(dev)
+        torch.cuda.nvtx.range_pop()
         barrier()
     clk = clocks.summary()
     if status.item() != 0:
@@ -323,8 +325,10 @@ def run_ours(args):
             dev_status=status, stream=stream), alg_bytes_step, "fp8z_adamw_requant_step_rowmajor")
         del w_row
 
+    torch.cuda.nvtx.range_push("aux_kernels")
     aux = None if (args.no_aux or len(shards) != 1) else time_aux_kernels(
         w, q, inv, params, dev, stream, peak, g=state["g"], fused=fused)
+    torch.cuda.nvtx.range_pop()
     if aux is not None:
         # the MXFP8 output variant of the same step (no column-major copy): codes
         # + one E8M0 byte per 32 elements, no block-wide amax
@@ -393,8 +397,10 @@ def run_ours(args):
             "rank0_gelem_s": round(r0_real / (r0_ms / 1e3) / 1e9, 4)}
 
     # ---- end to end through the C ABI with pinned host buffers
+    torch.cuda.nvtx.range_push("e2e")
     e2e = None if args.no_e2e else run_e2e(args, w, state, q, inv, wt, it, desc, pdev, params,
                                             shards, hp_kw, t, dev, ws)
+    torch.cuda.nvtx.range_pop()
 
     line = {
         "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": ws,

@@ -298,6 +298,7 @@ using namespace fp8z;
 
 extern "C" int fp8z_dequant(const uint8_t* w_fp8, const float* inv_scale, int64_t nblk, float* out,
                             int32_t* dev_status, void* stream) {
+    const fp8z::host::NvtxRange nvtx_range("fp8z_dequant");
     if (!w_fp8 || !inv_scale || !out || nblk < 0) return FP8Z_EINVAL;
     if (nblk > (INT64_MAX / kBlkElems) / 4) return FP8Z_EINVAL;
     if (!host::aligned(w_fp8, 16) || !host::aligned(out, 16) || !host::aligned(inv_scale, 4) ||
@@ -347,6 +348,7 @@ bool transpose_maps(const fp8z_param_entry& pe, const uint8_t* blocks, uint8_t* 
 extern "C" int fp8z_transpose_fp8(const uint8_t* w_fp8, const float* inv_scale,
                                   const fp8z_param_entry* entry, uint8_t* out, float* inv_scale_t,
                                   int32_t* dev_status, void* stream) {
+    const fp8z::host::NvtxRange nvtx_range("fp8z_transpose_fp8");
     if (!w_fp8 || !inv_scale || !entry || !out || !inv_scale_t) return FP8Z_EINVAL;
     const fp8z_param_entry& pe = *entry;
     if (pe.e < 1 || pe.rows < 1 || pe.cols < 1 || pe.blk_offset < 0) return FP8Z_EINVAL;
@@ -396,6 +398,7 @@ extern "C" int fp8z_transpose_fp8(const uint8_t* w_fp8, const float* inv_scale,
 }
 
 extern "C" int fp8z_e4m3_encode_bits(uint32_t first_bits, int64_t n, uint8_t* out, void* stream) {
+    const fp8z::host::NvtxRange nvtx_range("fp8z_e4m3_encode_bits");
     if (!out || n < 0 || (n & 3) != 0 || n > (int64_t(1) << 32)) return FP8Z_EINVAL;
     if (!host::aligned(out, 16)) return FP8Z_EALIGN;
     if (n == 0) return FP8Z_OK;
@@ -407,6 +410,7 @@ extern "C" int fp8z_e4m3_encode_bits(uint32_t first_bits, int64_t n, uint8_t* ou
 }
 
 extern "C" int fp8z_watchdog_selftest(int32_t* dev_status, int64_t timeout_ns, void* stream) {
+    const fp8z::host::NvtxRange nvtx_range("fp8z_watchdog_selftest");
     if (!dev_status || timeout_ns < 0 || timeout_ns > 10000000000LL) return FP8Z_EINVAL;
     if (!host::aligned(dev_status, 4)) return FP8Z_EALIGN;
     int sms = 0;

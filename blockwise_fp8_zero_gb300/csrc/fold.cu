@@ -248,10 +248,12 @@ int run(bool fold, const void* src, int32_t esz, const fp8z_param_entry* entry, 
 
 extern "C" int fp8z_fold(const void* src, int32_t elem_bytes, const fp8z_param_entry* entry,
                          void* blocks, int32_t* dev_status, void* stream) {
+    const fp8z::host::NvtxRange nvtx_range("fp8z_fold");
     return fp8z::run(true, src, elem_bytes, entry, blocks, dev_status, stream);
 }
 
 extern "C" int fp8z_unfold(const void* blocks, int32_t elem_bytes, const fp8z_param_entry* entry,
                            void* dst, int32_t* dev_status, void* stream) {
+    const fp8z::host::NvtxRange nvtx_range("fp8z_unfold");
     return fp8z::run(false, blocks, elem_bytes, entry, dst, dev_status, stream);
 }

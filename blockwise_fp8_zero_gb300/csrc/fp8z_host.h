@@ -4,10 +4,22 @@
 
 #include <cstdint>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "fp8z.h"
 
 namespace fp8z {
 namespace host {
+
+// A named NVTX range over one library call, so a profiler timeline shows each
+// call with the kernels it enqueued.  Header-only NVTX: without an attached
+// tool a push/pop pair costs a few nanoseconds.
+struct NvtxRange {
+    explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+    NvtxRange(const NvtxRange&) = delete;
+    NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 // Limit for every bounded device wait (2 s): far above any legitimate wait in
 // a step, far below anything that would look like a hung GPU.

@@ -17,6 +17,7 @@
 #include <vector>
 
 #include "fp8z.h"
+#include "fp8z_host.h"
 
 namespace {
 
@@ -58,6 +59,7 @@ extern "C" int fp8z_plan_shards(const fp8z_param_shape* shapes, int32_t nparams,
                                 int32_t split, fp8z_param_entry* params_out,
                                 fp8z_shard* shards_out, fp8z_block_desc* blocks_out,
                                 int64_t blocks_cap, fp8z_plan_summary* summary_out) {
+    const fp8z::host::NvtxRange nvtx_range("fp8z_plan_shards");
     if (nparams < 0 || dp < 1 || !params_out || !shards_out || !summary_out) return FP8Z_EINVAL;
     if (split != FP8Z_SPLIT_BLOCKWISE && split != FP8Z_SPLIT_PARAMWISE) return FP8Z_EINVAL;
     if (nparams > 0 && !shapes) return FP8Z_EINVAL;

@@ -319,6 +319,7 @@ using namespace fp8z;
 
 extern "C" int fp8z_quantize_rowwise(const float* x, int64_t rows, int64_t cols, int32_t pow2,
                                      uint8_t* q, float* s, void* stream) {
+    const fp8z::host::NvtxRange nvtx_range("fp8z_quantize_rowwise");
     if (!x || !q || !s || rows < 0 || cols < 0 || (cols % kTile) != 0 || (pow2 != 0 && pow2 != 1))
         return FP8Z_EINVAL;
     if (rows > (INT64_MAX / 4) / (cols > 0 ? cols : 1)) return FP8Z_EINVAL;
@@ -340,6 +341,7 @@ extern "C" int fp8z_quantize_rowwise(const float* x, int64_t rows, int64_t cols,
 
 extern "C" int fp8z_transpose_rowwise(const uint8_t* q, const float* s, int64_t rows, int64_t cols,
                                       uint8_t* q_t, float* s_t, void* stream) {
+    const fp8z::host::NvtxRange nvtx_range("fp8z_transpose_rowwise");
     if (!q || !s || !q_t || !s_t || rows < 0 || cols < 0 || rows % kTile || cols % kTile)
         return FP8Z_EINVAL;
     const int64_t ntiles = (rows / kTile) * (cols / kTile);

@@ -726,6 +726,7 @@ extern "C" int fp8z_adamw_requant_step(float* p, const float* g, float* m, float
                                        float* inv_scale_t, int64_t inv_scale_t_count,
                                        const fp8z_adamw_hparams* hp, int32_t* dev_status,
                                        void* stream) {
+    const fp8z::host::NvtxRange nvtx_range("fp8z_adamw_requant_step");
     if (!g || !w_fp8 || !inv_scale) return FP8Z_EINVAL;
     if (!host::aligned(g, 16) || !host::aligned(w_fp8, 16) || !host::aligned(inv_scale, 4))
         return FP8Z_EALIGN;
@@ -750,6 +751,7 @@ extern "C" int fp8z_adamw_requant_step_rowmajor(float* p, float* m, float* v, co
                                                 float* inv_scale_t, int64_t inv_scale_t_count,
                                                 const fp8z_adamw_hparams* hp, int32_t* dev_status,
                                                 void* stream) {
+    const fp8z::host::NvtxRange nvtx_range("fp8z_adamw_requant_step_rowmajor");
     if (!g_maps || !w_row || !inv_scale || !desc || !params || nparams <= 0 || w_row_bytes < 0)
         return FP8Z_EINVAL;
     if (!host::aligned(g_maps, 64) || !host::aligned(w_row, 16) || !host::aligned(inv_scale, 4))
@@ -771,6 +773,7 @@ extern "C" int fp8z_adamw_requant_step_mx(float* p, const float* g, float* m, fl
                                           int64_t blk_begin, int64_t nblk, const fp8z_block_desc* desc,
                                           const fp8z_adamw_hparams* hp, int32_t* dev_status,
                                           void* stream) {
+    const fp8z::host::NvtxRange nvtx_range("fp8z_adamw_requant_step_mx");
     if (!g || !w_fp8 || !mx_scale) return FP8Z_EINVAL;
     if (!host::aligned(g, 16) || !host::aligned(w_fp8, 16)) return FP8Z_EALIGN;
     StepArgs A;
@@ -785,6 +788,7 @@ extern "C" int fp8z_adamw_requant_step_mx(float* p, const float* g, float* m, fl
 
 extern "C" int fp8z_encode_grad_maps(const void* const* g_ptrs, const fp8z_param_entry* params,
                                      int32_t nparams, void* maps_out) {
+    const fp8z::host::NvtxRange nvtx_range("fp8z_encode_grad_maps");
     if (!g_ptrs || !params || !maps_out || nparams <= 0) return FP8Z_EINVAL;
     if (!host::aligned(maps_out, 64)) return FP8Z_EALIGN;
     auto enc = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(host::tensor_map_encoder());
