@@ -56,7 +56,10 @@ namespace {
 // dealing block rows fastest so the column-major writes of concurrent CTAs
 // continue each other (-0.6 %: the reads lose more page locality than the
 // column-major writes gain), one, two or four extra warps that do only the
-// column-major copy while the consumers move on (-3.8 %, -0.2 %, +0.1 %).
+// column-major copy while the consumers move on (-3.8 %, -0.2 %, +0.1 %),
+// the same 192 KB ring as twelve 8-row stages with warps 0-7 and 8-15 on
+// alternate stages (-0.9 %), and each warp loading its next stage into
+// registers before computing the current one (-0.3 %).
 //   FP8Z_RING             shared-memory stages in the ring
 //   FP8Z_ROWS_PER_WARP    block rows each consumer warp takes per stage
 //   FP8Z_STORE_STREAMING  1: p', m', v' stored with the streaming (.cs) hint
