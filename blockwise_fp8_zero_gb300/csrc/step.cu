@@ -456,6 +456,15 @@ __global__ void __launch_bounds__(kThreads, 1) fp8z_step_kernel(const StepArgs A
             for (int k = 0; k < kStagesPerBlock; ++k) {
                 if (has_next && k == kStagesPerBlock / 2) pinext = load_param(A, pnext);
                 if (!mbar_wait_bounded(empty0 + 8 * slot, phase ^ 1, wd)) goto drain;
+                // The consumers read this slot with plain loads and released it
+                // (release arrive, acquired by the wait above); the TMA refill is
+                // an async-proxy write, which that release/acquire alone does not
+                // order after those reads.  A proxy fence on the path between
+                // them does.  Without one, a variant that kept its loaded values
+                // unused for a stage read refilled data in every run; with this
+                // fence, or with one in every consumer before its arrive, none
+                // did, and this one costs no measurable time.
+                fence_proxy_async();
                 const uint32_t full = full0 + 8 * slot;
                 mbar_arrive_expect_tx(full, (kRowMajor && !gmap_ok) ? 3 * kTensorStageBytes : kStageBytes);
                 const uint32_t dst = ring0 + slot * kStageBytes;
@@ -538,11 +547,6 @@ __global__ void __launch_bounds__(kThreads, 1) fp8z_step_kernel(const StepArgs A
                 m4[r] = lds4(st + 2 * kStageElems + e0);
                 v4[r] = lds4(st + 3 * kStageElems + e0);
             }
-            // The slot is refilled by the TMA engine (async proxy) once every warp
-            // has arrived; the proxy fence orders this thread's generic reads of
-            // it before that write.  Without it a variant that kept the loaded
-            // values unused for a stage read refilled data in some runs.
-            fence_proxy_async();
             __syncwarp();
             if (lane == 0) mbar_arrive(empty0 + 8 * slot);
             if (++slot == kRing) { slot = 0; phase ^= 1; }
