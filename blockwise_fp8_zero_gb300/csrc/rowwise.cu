@@ -55,6 +55,28 @@ __device__ __forceinline__ float exp2i(int k) {
     return k >= -126 ? __uint_as_float(uint32_t(k + 127) << 23) : __uint_as_float(1u << (k + 149));
 }
 
+// Streaming 16-byte load through the non-coherent path with a 256-byte L2
+// fetch: the first load of a tile's 128-byte line also brings the next line
+// into L2.  On GB300 at 65536x7168 the quantizer ran 0.334 ms with it against
+// 0.358 ms with `.cs` loads (.cs or L1::no_allocate with the same 256-byte
+// fetch: 0.360 ms).  The input is read-only for the kernel's lifetime.
+__device__ __forceinline__ float4 ld_stream_l2_256(const float4* p) {
+    float4 r;
+    asm volatile("ld.global.nc.L2::256B.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(r.x), "=f"(r.y), "=f"(r.z), "=f"(r.w)
+                 : "l"(p));
+    return r;
+}
+
+// The same load for 16 bytes of codes.
+__device__ __forceinline__ uint4 ld_stream_l2_256(const uint4* p) {
+    uint4 r;
+    asm volatile("ld.global.nc.L2::256B.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+
 __device__ __forceinline__ float absmax4(float acc, float4 x) {
     return fmaxf(fmaxf(fmaxf(acc, fabsf(x.x)), fmaxf(fabsf(x.y), fabsf(x.z))), fabsf(x.w));
 }
@@ -64,7 +86,9 @@ __device__ __forceinline__ float absmax4(float acc, float4 x) {
 // (every load instruction reads whole 128-byte lines), the tile's amax needs
 // three shuffles, and the lane writes four 4-byte code words.  Measured on
 // GB300 at 65536x7168: 98 % of the copy bandwidth, against 82 % with one warp
-// per tile (five shuffles per four elements made that version issue-bound).
+// per tile (five shuffles per four elements made that version issue-bound);
+// 106 % with the loads' 256-byte L2 fetch (ld_stream_l2_256), the ceiling a
+// plain kernel with this 4:1 read:write mix reaches.
 __global__ void __launch_bounds__(256) quantize_rowwise_kernel(const float* __restrict__ x,
                                                                int64_t ntiles, int pow2,
                                                                uint8_t* __restrict__ q,
@@ -79,7 +103,7 @@ __global__ void __launch_bounds__(256) quantize_rowwise_kernel(const float* __re
         float4 v[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k)
-            v[k] = valid ? __ldcs(reinterpret_cast<const float4*>(x + t * kTile) + j + 8 * k)
+            v[k] = valid ? ld_stream_l2_256(reinterpret_cast<const float4*>(x + t * kTile) + j + 8 * k)
                          : make_float4(0.f, 0.f, 0.f, 0.f);
         float a = 0.0f;
 #pragma unroll
@@ -242,7 +266,9 @@ __device__ __forceinline__ void tile_ratios(const float* s, int64_t i, int64_t j
 // rows 4l..4l+3 with their ratios, a warp writing 128 contiguous bytes of one
 // output row per store.  Consecutive CTAs take consecutive row tiles of one
 // strip, so their output rows continue each other in memory.  Measured on
-// GB300 at 65536x7168: 0.159 ms with three CTAs per SM (80 registers; 0.162
+// GB300 at 65536x7168: 0.150 ms with the staging loads' 256-byte L2 fetch
+// (ld_stream_l2_256; 0.158 ms with `.cs` loads), three CTAs per SM (80
+// registers; with `.cs` loads 0.162
 // ms at 64 registers and four CTAs, 0.175 ms at 93 and two; before the
 // one-stage transpose, 0.192 ms at 48 registers and five); before that,
 // 0.170 against 0.162 ms when all eight warps computed the same ratios (four
@@ -283,7 +309,7 @@ __global__ void __launch_bounds__(256, 3) transpose_rowwise_kernel(const uint8_t
 #pragma unroll
     for (int it = 0; it < kIters; ++it) {
         const int idx = it * 256 + tid;
-        buf[it] = __ldcs(src + (idx / kChunks) * (C / 16) + idx % kChunks);
+        buf[it] = ld_stream_l2_256(src + (idx / kChunks) * (C / 16) + idx % kChunks);
     }
     if (warp < kW) tile_ratios(s, i, jw + warp, ntc, ntr, st, lane, ratios[warp]);
 #pragma unroll
