@@ -125,13 +125,19 @@ def _check(fn, rc):
 
 
 def _dptr(t, dtype=None, name="tensor"):
-    """Device pointer of a contiguous CUDA tensor (None -> NULL)."""
+    """Device pointer of a contiguous CUDA tensor on the current device (None
+    -> NULL).  The library launches on the current device, so a tensor of
+    another GPU is refused here rather than read through a foreign pointer."""
     if t is None:
         return None
     if not t.is_cuda or not t.is_contiguous():
         raise ValueError(f"{name} must be a contiguous CUDA tensor")
     if dtype is not None and t.dtype != dtype:
         raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    import torch
+    cur = torch.cuda.current_device()
+    if t.device.index is not None and t.device.index != cur:
+        raise ValueError(f"{name} is on {t.device}, but the current device is cuda:{cur}")
     return t.data_ptr()
 
 
