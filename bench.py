@@ -615,7 +615,10 @@ def run_e2e(args, w, state, q, inv, wt, it, desc, pdev, params, shards, hp_kw, t
             units.append((b0, nb_e, t0, int(pe["rows"]) * int(pe["cols"]), s0))
     nunits = len(units)
     per_unit_host = units[0][1] * BLK * 4 + units[0][1] * BLK * (2 if w.transposed else 1)
-    budget = max(1, int((host_mem_gb() * 1e9 * 0.5) // max(per_unit_host, 1)))
+    # pinned host buffers: at most half of the host's available memory, shared
+    # by every rank of this node
+    local_ranks = max(1, int(os.environ.get("LOCAL_WORLD_SIZE", "1")))
+    budget = max(1, int((host_mem_gb() * 1e9 * 0.5 / local_ranks) // max(per_unit_host, 1)))
     if budget < nunits:
         units = units[:budget]
     e_blocks = sum(u[1] for u in units)
