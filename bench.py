@@ -405,6 +405,8 @@ def run_ours(args):
     line = {
         "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 4),
+        "median_ms_per_step": round(float(np.median(per_step_ms)), 4),
+        "min_max_ms_per_step": [round(min(per_step_ms), 4), round(max(per_step_ms), 4)],
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic",
         "config": {"workload": w.name, "params": len(w.shapes), "elements": real, "blocks": nblk_run,

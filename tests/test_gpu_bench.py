@@ -39,6 +39,8 @@ def test_bench_line_schema():
     assert abs(r["frac"] - r["achieved"] / r["peak"]) < 1e-3
     assert abs(d["value"] - d["config"]["elements"] / (d["ms_per_step"] / 1e3) / 1e9) < 0.01 * d["value"]
     assert d["gpu_launches"] == d["steps"]
+    lo, hi = d["min_max_ms_per_step"]
+    assert 0 < lo <= d["median_ms_per_step"] <= hi
     assert {"sm_mhz", "sm_max_mhz", "reasons"} <= set(d["clocks"])
     e = d["e2e"]
     n = 7168 * 7168
