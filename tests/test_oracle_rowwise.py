@@ -93,11 +93,17 @@ def test_transpose_is_an_exponent_shift_with_pow2_scales(oracle):
             assert np.all(st[j * 128:(j + 1) * 128, i] == s[i * 128:(i + 1) * 128, j].max())
 
 
-def test_transpose_matches_definition_including_underflow(oracle):
+@pytest.mark.parametrize("pow2", [True, False])
+def test_transpose_matches_definition_including_underflow(oracle, pow2):
+    """Each transposed code is the nearest E4M3 value (brute force) to
+    decode(q) * (s_r / s'), the ratio rounded once to float32 (a float64
+    quotient of two floats rounds to the correctly rounded float quotient) and
+    the product once more; with amax/448 scales the ratios are not powers of
+    two, so almost every code is re-rounded."""
     rng = np.random.default_rng(4)
     x = _act(rng, 128, 256)
     x[7] *= 1e4                                # one row with a much larger scale
-    q, s = oracle.quantize_rowwise(x, pow2=True)
+    q, s = oracle.quantize_rowwise(x, pow2=pow2)
     qt, st = oracle.transpose_rowwise(q, s)
     dec = finite_e4m3_table()
     vals = np.where(q & 0x80, -1.0, 1.0) * dec[q & 0x7F]
