@@ -34,6 +34,10 @@
  *     [nblocks,128,128] fp32, row-major inside each block; byte buffers the
  *     same layout of E4M3 codes; scale buffers one fp32 per block.
  *   - Return codes are fp8z_status values; fp8z_status_string() names them.
+ *   - The device calls may be captured in a CUDA graph once the same call has
+ *     run eagerly on the device (that first call sets the kernels' launch
+ *     attributes); scalar arguments such as the hyper-parameters are captured
+ *     by value.
  */
 #ifndef FP8Z_H
 #define FP8Z_H
