@@ -157,3 +157,69 @@ def test_rowwise_activation_full(oracle, pow2):
         assert np.array_equal(qt[j * 128:(j + 1) * 128, i * 128:(i + 1) * 128].cpu().numpy(), qto), (i, j)
         assert np.array_equal(stt[j * 128:(j + 1) * 128, i:i + 1].cpu().numpy().view(np.uint32),
                               sto.view(np.uint32)), (i, j)
+
+
+def test_flat6e9_layout_kernels_full(oracle):
+    """Dequant, the standalone column-major copy, and fold/unfold of the FP32 grad
+    and of the E4M3 codes, each over the whole 117 x 7168^2 param as the
+    benchmark times them: sampled blocks against the oracle (dequant) or the
+    block itself (the copy and unfold are exact byte permutations), and
+    fold(unfold(x)) == x over every byte."""
+    w = workloads.get("flat6e9")
+    params, shards, blocks, summ = fp8z.fp8z_plan_shards(w.shapes, w.dp, w.split)
+    cap = int(summ["capacity_blocks"])
+    real = int(summ["real_elems"])
+    _need(cap * BLK * (16 + 1 + 4 + 4))
+    dev = torch.device("cuda")
+    state = workloads.make_state(w, blocks, dev, seed=4)
+    q = torch.zeros(cap * BLK, dtype=torch.uint8, device=dev)
+    inv = torch.zeros(cap, device=dev)
+    desc = fp8z.table_to_device(blocks, dev)
+    fp8z.fp8z_adamw_requant_step(state["p"], state["g"], state["m"], state["v"], q, inv, 0, cap,
+                                 fp8z.hparams(**w.hp), desc=desc)
+    for k in "pmv":
+        del state[k]
+    torch.cuda.empty_cache()
+    idx = _sample(cap, n=400, seed=2)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    pe = params[0]
+    E, H, W = int(pe["e"]), int(pe["rows"]), int(pe["cols"])
+    # dequant
+    out = torch.empty(cap * BLK, device=dev)
+    fp8z.fp8z_dequant(q, inv, cap, out, dev_status=st)
+    torch.cuda.synchronize()
+    qs, invs = _gather(q, idx, BLK), inv[torch.from_numpy(idx).to(dev)].cpu().numpy()
+    want = oracle.dequant(qs, invs, idx.size)
+    assert np.array_equal(_gather(out, idx, BLK).view(np.uint32), want.view(np.uint32))
+    del out
+    torch.cuda.empty_cache()
+    # standalone column-major copy
+    qt = torch.empty(real, dtype=torch.uint8, device=dev)
+    it = torch.empty(E * int(pe["hb"]) * int(pe["wb"]), device=dev)
+    fp8z.fp8z_transpose_fp8(q, inv, pe, qt, it, dev_status=st)
+    torch.cuda.synchronize()
+    colm, itv = qt.view(E, W, H), it.view(E, int(pe["wb"]), int(pe["hb"]))
+    for j, b in enumerate(idx[:200]):
+        bd = blocks[b]
+        e, r0, c0 = int(bd["e"]), int(bd["brow"]) * 128, int(bd["bcol"]) * 128
+        blk = qs[j * BLK:(j + 1) * BLK].reshape(128, 128)
+        assert np.array_equal(colm[e, c0:c0 + 128, r0:r0 + 128].cpu().numpy(), blk.T), int(b)
+        assert itv[e, int(bd["bcol"]), int(bd["brow"])].item() == invs[j]
+    del qt, it
+    # unfold / fold of the E4M3 codes and of the FP32 grad
+    for name, folded in (("e4m3", q), ("f32", state["g"])):
+        rm = torch.empty(real, dtype=folded.dtype, device=dev)
+        fp8z.fp8z_unfold(folded, pe, rm, dev_status=st)
+        back = torch.zeros_like(folded)
+        fp8z.fp8z_fold(rm, pe, back, dev_status=st)
+        torch.cuda.synchronize()
+        assert torch.equal(back.view(torch.uint8), folded.view(torch.uint8)), name
+        rmv = rm.view(E, H, W)
+        fb = folded.view(-1, 128, 128)
+        for b in idx[:100]:
+            bd = blocks[b]
+            e, r0, c0 = int(bd["e"]), int(bd["brow"]) * 128, int(bd["bcol"]) * 128
+            assert torch.equal(rmv[e, r0:r0 + 128, c0:c0 + 128], fb[int(b)]), (name, int(b))
+        del rm, back
+        torch.cuda.empty_cache()
+    assert st.item() == 0, fp8z.fp8z_status_string(st.item())
