@@ -76,6 +76,15 @@ class Case:
             self.wt = self.it = None
         self.status = torch.zeros(1, dtype=torch.int32, device=device)
         self.processed = np.zeros(self.cap, bool)
+        self._oracle_plan = None
+
+    def oracle_tables(self, oracle):
+        """The oracle's own planner tables (params, blocks) for this layout: the
+        oracle's inputs never come from the library."""
+        if self._oracle_plan is None:
+            op, _, ob, _ = oracle.plan_shards(self.shapes, self.dp, self.split)
+            self._oracle_plan = (op, ob)
+        return self._oracle_plan
 
     def step(self, hp, ranges=None, use_desc=True):
         """Run the CUDA step over the given (begin, count) block ranges
@@ -99,10 +108,9 @@ class Case:
         p, g, m, v = (self.host[k].copy() for k in "pgmv")
         wt = np.zeros(self.t_bytes, np.uint8) if self.transposed else None
         it = np.zeros(self.t_scales, np.float32) if self.transposed else None
-        params = None
-        if self.transposed:
-            params = np.ascontiguousarray(self.params).view(oracle.PARAM_ENTRY)
-        desc = np.ascontiguousarray(self.blocks).view(oracle.BLOCK_DESC) if use_desc else None
+        op, ob = self.oracle_tables(oracle)
+        params = op if self.transposed else None
+        desc = ob if use_desc else None
         q, inv = oracle_blocks(oracle, hp, p, g, m, v, desc, params, wt, it)
         return dict(p=p, m=m, v=v, q=q, inv=inv, wt=wt, it=it)
 

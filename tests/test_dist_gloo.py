@@ -58,7 +58,8 @@ def _worker(rank, world, port, q):
         p, g, m, v = (st[k][sl].copy() for k in "pgmv")
         q_loc = np.zeros(C * BLK, np.uint8)
         inv_loc = np.zeros(C, np.float32)
-        desc = np.ascontiguousarray(blocks[b0:b0 + C]).view(oracle.BLOCK_DESC)
+        o_blocks = oracle.plan_shards(SHAPES, world, 0)[2]          # the oracle's own plan
+        desc = np.ascontiguousarray(o_blocks[b0:b0 + C])
         oracle.adamw_requant_step(p, g, m, v, q_loc, inv_loc, 0, nb, oracle.Hparams.make(step=4),
                                   desc=desc)
         # the exchange after the update: all-gather the shard's bytes and scales
@@ -74,7 +75,7 @@ def _worker(rank, world, port, q):
         s_ref = np.zeros(cap, np.float32)
         oracle.adamw_requant_step(p2, g2, m2, v2, q_ref, s_ref, 0, int(summ["total_blocks"]),
                                   oracle.Hparams.make(step=4),
-                                  desc=np.ascontiguousarray(blocks).view(oracle.BLOCK_DESC))
+                                  desc=o_blocks)
         data = blocks["param"] >= 0
         assert np.array_equal(whole_q, q_ref)
         assert np.array_equal(whole_s[data], s_ref[data])

@@ -78,12 +78,13 @@ def run_sampled(oracle, w, one_launch=False):
     assert st.item() == 0, fp8z.fp8z_status_string(st.item())
     # checked in chunks of blocks, so the host holds the inputs of the sample
     # (gathered before the step) and one chunk of outputs at a time
+    o_blocks = oracle.plan_shards(w.shapes, w.dp, w.split)[2]      # the oracle's own plan
     for c0 in range(0, idx.size, CHUNK):
         ii = idx[c0:c0 + CHUNK]
         got = {k: _gather(state[k], ii, BLK) for k in "pmv"}
         got["q"] = _gather(q, ii, BLK)
         got["inv"] = inv[torch.from_numpy(ii).to(dev)].cpu().numpy()
-        d = np.ascontiguousarray(blocks[ii]).view(oracle.BLOCK_DESC)
+        d = np.ascontiguousarray(o_blocks[ii])
         sl = slice(c0 * BLK, (c0 + ii.size) * BLK)
         pc = {k: pre[k][sl] for k in "pgmv"}
         qc, invc = oracle_blocks(oracle, hp, pc["p"], pc["g"], pc["m"], pc["v"], d)

@@ -64,7 +64,7 @@ def test_flat6e9_mxfp8_full(oracle):
     assert st.item() == 0, fp8z.fp8z_status_string(st.item())
     qo = np.zeros(idx.size * BLK, np.uint8)
     so = np.zeros(idx.size * 512, np.uint8)
-    d = np.ascontiguousarray(blocks[idx]).view(oracle.BLOCK_DESC)
+    d = np.ascontiguousarray(oracle.plan_shards(w.shapes, w.dp, w.split)[2][idx])   # the oracle's own plan
     oracle.adamw_requant_step_mx(pre["p"], pre["g"], pre["m"], pre["v"], qo, so, 0, idx.size,
                                  oracle.Hparams.make(**w.hp), desc=d)
     for k in "pmv":
@@ -106,7 +106,7 @@ def test_flat6e9_rowmajor_full(oracle):
     assert st.item() == 0, fp8z.fp8z_status_string(st.item())
     qo = np.zeros(idx.size * BLK, np.uint8)
     invo = np.zeros(idx.size, np.float32)
-    d = np.ascontiguousarray(blocks[idx]).view(oracle.BLOCK_DESC)
+    d = np.ascontiguousarray(oracle.plan_shards(w.shapes, w.dp, w.split)[2][idx])   # the oracle's own plan
     oracle.adamw_requant_step(pre["p"], pre["g"], pre["m"], pre["v"], qo, invo, 0, idx.size,
                               oracle.Hparams.make(**w.hp), desc=d)
     for k in "pmv":
@@ -151,8 +151,10 @@ def test_rowwise_activation_full(oracle, pow2):
     assert np.array_equal(s[ri].cpu().numpy().view(np.uint32), so.view(np.uint32))
     for _ in range(24):
         i, j = int(rng.integers(T // 128)), int(rng.integers(Hd // 128))
-        qin = q[i * 128:(i + 1) * 128, j * 128:(j + 1) * 128].cpu().numpy()
-        sin = s[i * 128:(i + 1) * 128, j:j + 1].cpu().numpy()
+        # the oracle transposes its own quantization of the tile's 128 rows (the
+        # 1x128 tiles of a 128x128 block are the row tiles of that block)
+        xin = x[i * 128:(i + 1) * 128, j * 128:(j + 1) * 128].cpu().numpy()
+        qin, sin = oracle.quantize_rowwise(xin, pow2=pow2)
         qto, sto = oracle.transpose_rowwise(qin, sin)
         assert np.array_equal(qt[j * 128:(j + 1) * 128, i * 128:(i + 1) * 128].cpu().numpy(), qto), (i, j)
         assert np.array_equal(stt[j * 128:(j + 1) * 128, i:i + 1].cpu().numpy().view(np.uint32),
@@ -162,8 +164,9 @@ def test_rowwise_activation_full(oracle, pow2):
 def test_flat6e9_layout_kernels_full(oracle):
     """Dequant, the standalone column-major copy, and fold/unfold of the FP32 grad
     and of the E4M3 codes, each over the whole 117 x 7168^2 param as the
-    benchmark times them: sampled blocks against the oracle (dequant) or the
-    block itself (the copy and unfold are exact byte permutations), and
+    benchmark times them: sampled blocks of a seeded dequant input against the
+    oracle; the copy and unfold against the block itself (exact byte
+    permutations of the step's output, a property at any size, no oracle); and
     fold(unfold(x)) == x over every byte."""
     w = workloads.get("flat6e9")
     params, shards, blocks, summ = fp8z.fp8z_plan_shards(w.shapes, w.dp, w.split)
@@ -184,14 +187,21 @@ def test_flat6e9_layout_kernels_full(oracle):
     st = torch.zeros(1, dtype=torch.int32, device=dev)
     pe = params[0]
     E, H, W = int(pe["e"]), int(pe["rows"]), int(pe["cols"])
-    # dequant
-    out = torch.empty(cap * BLK, device=dev)
-    fp8z.fp8z_dequant(q, inv, cap, out, dev_status=st)
-    torch.cuda.synchronize()
     qs, invs = _gather(q, idx, BLK), inv[torch.from_numpy(idx).to(dev)].cpu().numpy()
-    want = oracle.dequant(qs, invs, idx.size)
+    # dequant of every block: seeded codes (no NaN code) and per-block inverse
+    # scales, so the oracle's inputs come from the generator, not the library
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(9)
+    qd = torch.randint(0, 256, (cap * BLK,), dtype=torch.uint8, device=dev, generator=gen)
+    qd[(qd & 0x7F) == 0x7F] = 0
+    invd = torch.exp2(torch.randint(-30, 30, (cap,), device=dev, generator=gen).float()) * \
+        (1.0 + torch.rand(cap, device=dev, generator=gen))
+    out = torch.empty(cap * BLK, device=dev)
+    fp8z.fp8z_dequant(qd, invd, cap, out, dev_status=st)
+    torch.cuda.synchronize()
+    want = oracle.dequant(_gather(qd, idx, BLK), invd[torch.from_numpy(idx).to(dev)].cpu().numpy(), idx.size)
     assert np.array_equal(_gather(out, idx, BLK).view(np.uint32), want.view(np.uint32))
-    del out
+    del out, qd, invd
     torch.cuda.empty_cache()
     # standalone column-major copy
     qt = torch.empty(real, dtype=torch.uint8, device=dev)

@@ -244,7 +244,7 @@ def test_dense_h7168_full(oracle):
                                      desc=desc, dev_status=st)
     torch.cuda.synchronize()
     assert st.item() == 0
-    d = np.ascontiguousarray(blocks).view(oracle.BLOCK_DESC)
+    d = oracle.plan_shards(w.shapes, w.dp, w.split)[2]       # the oracle's own plan
     qo, invo = oracle_blocks(oracle, hp, host["p"], host["g"], host["m"], host["v"], d)
     got = dict(p=dev["p"].cpu().numpy(), m=dev["m"].cpu().numpy(), v=dev["v"].cpu().numpy(),
                q=q.cpu().numpy(), inv=inv.cpu().numpy())
@@ -252,13 +252,14 @@ def test_dense_h7168_full(oracle):
 
 
 def test_dequant(oracle):
+    # codes and scales of a step, made by the oracle and uploaded: no input of
+    # the oracle comes from the library
     c = Case([(1, 384, 640)], dp=1, seed=4)
-    hp = fp8z.hparams(step=2)
-    c.step(hp)
+    ref = c.oracle(oracle, fp8z.hparams(step=2))
     out = torch.empty(c.cap * BLK, dtype=torch.float32, device="cuda")
-    fp8z.fp8z_dequant(c.w_fp8, c.inv, c.cap, out)
+    fp8z.fp8z_dequant(torch.from_numpy(ref["q"]).cuda(), torch.from_numpy(ref["inv"]).cuda(), c.cap, out)
     torch.cuda.synchronize()
-    want = oracle.dequant(c.w_fp8.cpu().numpy(), c.inv.cpu().numpy(), c.cap)
+    want = oracle.dequant(ref["q"], ref["inv"], c.cap)
     assert np.array_equal(out.cpu().numpy().view(np.uint32), want.view(np.uint32))
 
 
@@ -287,18 +288,20 @@ def test_dequant_every_code(oracle, nblk):
                                    (2, 272, 200), (1, 16, 16), (8, 1024, 1152), (40, 512, 512),
                                    (3, 1040, 7)])
 def test_standalone_transpose(oracle, shape):
+    # the codes and scales of a step, made by the oracle, go to both sides
     c = Case([shape], dp=1, seed=6)
-    c.step(fp8z.hparams(step=3))
+    ref = c.oracle(oracle, fp8z.hparams(step=3))
     E, H, W = shape
     pe = c.params[0]
     out = torch.full((E * W * H,), 0xA5, dtype=torch.uint8, device="cuda")
     it = torch.zeros(E * int(pe["wb"]) * int(pe["hb"]), dtype=torch.float32, device="cuda")
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
-    fp8z.fp8z_transpose_fp8(c.w_fp8, c.inv, pe, out, it, dev_status=st)
+    fp8z.fp8z_transpose_fp8(torch.from_numpy(ref["q"]).cuda(), torch.from_numpy(ref["inv"]).cuda(), pe, out,
+                            it, dev_status=st)
     torch.cuda.synchronize()
     assert st.item() == 0, fp8z.fp8z_status_string(st.item())
-    ent = np.ascontiguousarray(c.params).view(oracle.PARAM_ENTRY)[0]
-    wt, wit = oracle.transpose_fp8(c.w_fp8.cpu().numpy(), c.inv.cpu().numpy(), ent)
+    ent = c.oracle_tables(oracle)[0][0]
+    wt, wit = oracle.transpose_fp8(ref["q"], ref["inv"], ent)
     assert np.array_equal(out.cpu().numpy(), wt.ravel())
     assert np.array_equal(it.cpu().numpy(), wit.ravel())
 
@@ -380,7 +383,7 @@ def test_mxfp8_step(oracle, shapes):
     sc = np.zeros(c.cap * 512, np.uint8)
     oracle.adamw_requant_step_mx(p, g, m, v, q, sc, 0, int(c.summary["total_blocks"]),
                                  oracle.Hparams.make(step=6),
-                                 desc=np.ascontiguousarray(c.blocks).view(oracle.BLOCK_DESC))
+                                 desc=c.oracle_tables(oracle)[1])
     for k, want in (("p", p), ("m", m), ("v", v)):
         assert np.array_equal(c.dev[k].cpu().numpy().view(np.uint32), want.view(np.uint32)), k
     assert np.array_equal(c.w_fp8.cpu().numpy(), q)
@@ -410,7 +413,7 @@ def test_mxfp8_extreme_magnitudes(oracle, step):
     q = np.zeros(c.cap * BLK, np.uint8)
     sc = np.zeros(c.cap * 512, np.uint8)
     oracle.adamw_requant_step_mx(p, g, m, v, q, sc, 0, c.cap, oracle.Hparams.make(step=step),
-                                 desc=np.ascontiguousarray(c.blocks).view(oracle.BLOCK_DESC))
+                                 desc=c.oracle_tables(oracle)[1])
     for k, want in (("p", p), ("m", m), ("v", v)):
         a = c.dev[k].cpu().numpy()
         assert np.all((a.view(np.uint32) == want.view(np.uint32)) | (np.isnan(a) & np.isnan(want))), k
@@ -439,7 +442,7 @@ def test_mxfp8_hyperparameters(oracle, seed):
     sc = np.zeros(c.cap * 512, np.uint8)
     oracle.adamw_requant_step_mx(p, g, m, v, q, sc, 0, int(c.summary["total_blocks"]),
                                  oracle.Hparams.make(**kw),
-                                 desc=np.ascontiguousarray(c.blocks).view(oracle.BLOCK_DESC))
+                                 desc=c.oracle_tables(oracle)[1])
     for k, want in (("p", p), ("m", m), ("v", v)):
         assert np.array_equal(c.dev[k].cpu().numpy().view(np.uint32), want.view(np.uint32)), k
     assert np.array_equal(c.w_fp8.cpu().numpy(), q)

@@ -70,10 +70,9 @@ def run_case(oracle, shapes, dp, split=0, transposed=False, step=5, seed=0, bad_
     assert st.item() == 0, fp8z.fp8z_status_string(st.item())
     wt_o = np.zeros(t_bytes, np.uint8) if transposed else None
     it_o = np.zeros(t_scales, np.float32) if transposed else None
-    q_o, inv_o = oracle_blocks(oracle, hp, host["p"], g_fold, host["m"], host["v"],
-                               np.ascontiguousarray(blocks).view(oracle.BLOCK_DESC),
-                               np.ascontiguousarray(params).view(oracle.PARAM_ENTRY) if transposed else None,
-                               wt_o, it_o)
+    o_params, _, o_blocks, _ = oracle.plan_shards(shapes, dp, split)    # the oracle's own plan
+    q_o, inv_o = oracle_blocks(oracle, hp, host["p"], g_fold, host["m"], host["v"], o_blocks,
+                               o_params if transposed else None, wt_o, it_o)
     for k in "pmv":
         assert np.array_equal(d[k].cpu().numpy().view(np.uint32), host[k].view(np.uint32)), k
     data = blocks["param"] >= 0

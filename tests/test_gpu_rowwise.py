@@ -56,13 +56,14 @@ def test_quantize_rowwise(oracle, shape, pow2):
 @pytest.mark.parametrize("pow2", [True, False])
 def test_transpose_rowwise(oracle, shape, pow2):
     x = _act(*shape, seed=shape[1])
-    q, s = _gpu_quantize(x, pow2)
+    # the oracle's row-wise codes and scales go to both sides
+    qo, so = oracle.quantize_rowwise(x.numpy(), pow2=pow2)
     R, C = shape
     qt = torch.empty(C, R, dtype=torch.uint8, device="cuda")
     st = torch.empty(C, R // 128, device="cuda")
-    fp8z.fp8z_transpose_rowwise(q, s, qt, st)
+    fp8z.fp8z_transpose_rowwise(torch.from_numpy(qo).cuda(), torch.from_numpy(so).cuda(), qt, st)
     torch.cuda.synchronize()
-    qto, sto = oracle.transpose_rowwise(q.cpu().numpy(), s.cpu().numpy())
+    qto, sto = oracle.transpose_rowwise(qo, so)
     assert np.array_equal(st.cpu().numpy().view(np.uint32), sto.view(np.uint32))
     assert np.array_equal(qt.cpu().numpy(), qto)
 
