@@ -428,7 +428,7 @@ def run_ours(args):
         "clocks": clk,
         "e2e": e2e,
     }
-    if rank == 0 and not args.no_cpu_baseline:
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:      # the host baseline at N = 1 only
         line["cpu_baseline"] = cpu_baseline(w, hp_kw, args)
     if rank == 0:
         print(json.dumps(line), flush=True)
