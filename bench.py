@@ -415,6 +415,7 @@ def run_ours(args):
                    "dp_shards": w.dp, "column_major_copy": w.transposed, "step": step0,
                    "l2": f"state {cap * BLK * 16 / 1e9:.0f} GB >> 129 MB L2: no flush between steps",
                    "launches_per_step": launches_per_step, "scaled": scaled_note,
+                   "parallelism": f"{ws} independent replicas, one per GPU" if ws > 1 else "one GPU",
                    "hbm_gbs": round(achieved, 1),
                    "frac_of_nominal_8tbs": round(achieved / NOMINAL_HBM_GBS, 4)},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
