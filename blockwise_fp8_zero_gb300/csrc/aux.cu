@@ -87,9 +87,11 @@ __global__ void __launch_bounds__(kDqThreads) dequant_kernel(const uint8_t* __re
         }
     }
     if (tid == 0) {
-        if (k < count)                                     // gave up: let the issued loads land
+        // gave up at block k: blocks k .. k + kDqStages - 1 may have loads in
+        // flight (every earlier load was waited for); let them land
+        if (k < count)
             for (int64_t kk = k; kk < count && kk < k + kDqStages; ++kk)
-                mbar_wait_bounded(bar0 + 8 * int(kk % kDqStages), uint32_t((kk / kDqStages) & 1), wd, false);
+                mbar_wait_drain(bar0 + 8 * int(kk % kDqStages), uint32_t((kk / kDqStages) & 1), dev_status);
         bulk_wait_all();
     }
 }
@@ -252,9 +254,11 @@ __global__ void __launch_bounds__(256) transpose_tma_kernel(const __grid_constan
         }
     }
     if (tid == 0) {
-        if (k < count)                                     // gave up: let the issued loads land
+        // gave up at block k: blocks k .. k + kTStages - 1 may have loads in
+        // flight (every earlier load was waited for); let them land
+        if (k < count)
             for (int64_t kk = k; kk < count && kk < k + kTStages; ++kk)
-                mbar_wait_bounded(bar0 + 8 * int(kk % kTStages), uint32_t((kk / kTStages) & 1), wd, false);
+                mbar_wait_drain(bar0 + 8 * int(kk % kTStages), uint32_t((kk / kTStages) & 1), T.dev_status);
         bulk_wait_all();
     }
 }
@@ -312,7 +316,7 @@ extern "C" int fp8z_dequant(const uint8_t* w_fp8, const float* inv_scale, int64_
     if (rc != FP8Z_OK) return rc;
     const unsigned grid = unsigned(nblk < sms ? nblk : sms);
     dequant_kernel<<<grid, kDqThreads, kDqSmemBytes, static_cast<cudaStream_t>(stream)>>>(
-        w_fp8, inv_scale, nblk, out, dev_status, host::kDefaultTimeoutNs);
+        w_fp8, inv_scale, nblk, out, dev_status, host::wait_limit_ns());
     return cudaGetLastError() == cudaSuccess ? FP8Z_OK : FP8Z_ECUDA;
 }
 
@@ -380,7 +384,7 @@ extern "C" int fp8z_transpose_fp8(const uint8_t* w_fp8, const float* inv_scale,
         T.hb = pe.hb;
         T.wb = pe.wb;
         T.dev_status = dev_status;
-        T.timeout_ns = host::kDefaultTimeoutNs;
+        T.timeout_ns = host::wait_limit_ns();
         transpose_tma_kernel<<<unsigned(nb < cap ? nb : cap), 256, kTSmemBytes, st>>>(in_map, out_map, T);
         return cudaGetLastError() == cudaSuccess ? FP8Z_OK : FP8Z_ECUDA;
     }

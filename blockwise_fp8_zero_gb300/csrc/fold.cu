@@ -114,9 +114,10 @@ __global__ void __launch_bounds__(32) fold_tma_kernel(const __grid_constant__ CU
         }
         const int s = int(i % nbuf);
         if (!mbar_wait_bounded(bar0 + 8 * s, uint32_t((i / nbuf) & 1), wd)) {
-            // let every load still in flight land before the CTA leaves
-            for (int64_t k = i + 1; k < count && k <= j; ++k)
-                mbar_wait_bounded(bar0 + 8 * int(k % nbuf), uint32_t((k / nbuf) & 1), wd, false);
+            // let every load still in flight land before the CTA leaves:
+            // block i (the one that timed out) up to the newest issued, j
+            for (int64_t k = i; k < count && k <= j; ++k)
+                mbar_wait_drain(bar0 + 8 * int(k % nbuf), uint32_t((k / nbuf) & 1), F.dev_status);
             bulk_wait_all();
             return;
         }
@@ -200,7 +201,7 @@ int run(bool fold, const void* src, int32_t esz, const fp8z_param_entry* entry, 
             const int nbuf = ring / (kBlkElems * esz);
             static_assert(kRingBytesF32 / (kBlkElems * 4) - 1 - kStoreLagF32 >= 1, "FP32 ring too small");
             static_assert(kRingBytesU8 / kBlkElems - 1 - kStoreLagU8 >= 1, "byte ring too small");
-            FoldArgs F{flat, pe.hb, pe.wb, nblk, esz, nbuf, dev_status, host::kDefaultTimeoutNs};
+            FoldArgs F{flat, pe.hb, pe.wb, nblk, esz, nbuf, dev_status, host::wait_limit_ns()};
             const int smem = ring + nbuf * 8 + 16;
             const void* k = fold ? (f32 ? reinterpret_cast<const void*>(&fold_tma_kernel<true, kStoreLagF32>)
                                         : reinterpret_cast<const void*>(&fold_tma_kernel<true, kStoreLagU8>))

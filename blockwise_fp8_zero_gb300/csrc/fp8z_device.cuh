@@ -68,17 +68,37 @@ __device__ __forceinline__ void report_status(int32_t* dev_status, int32_t code)
 // Wait for `parity` on `bar`, for at most wd.timeout_ns nanoseconds.  Returns
 // false (after raising the CTA's abort flag and reporting FP8Z_ETIMEOUT) when
 // the limit is reached, or when another thread of the CTA has already
-// aborted and honor_abort is set.  Never spins without a limit.
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
-                                                  const Watchdog& wd, bool honor_abort = true) {
+// aborted.  Never spins without a limit.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, const Watchdog& wd) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
-        if (honor_abort && *wd.abort_flag) return false;
+        if (*wd.abort_flag) return false;
         if (global_timer_ns() - t0 > static_cast<uint64_t>(wd.timeout_ns)) {
             *wd.abort_flag = 1;
             report_status(wd.dev_status, FP8Z_ETIMEOUT);
+            return false;
+        }
+    }
+}
+
+// Limit for the waits of an abort path: a CTA that gave up still lets every
+// bulk copy it issued land before it exits, so the copy engine never writes
+// shared memory the CTA no longer owns.  A copy from a valid address always
+// completes, so this limit is far above any real wait, and it is separate from
+// the normal limit: a short normal limit never shortens a drain.
+constexpr int64_t kDrainLimitNs = 20000000000LL;   // 20 s
+
+// Wait for `parity` on `bar` on an abort path: ignores the CTA's abort flag,
+// gives up only after kDrainLimitNs (reporting FP8Z_ETIMEOUT).
+__device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, int32_t* dev_status) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (global_timer_ns() - t0 > static_cast<uint64_t>(kDrainLimitNs)) {
+            report_status(dev_status, FP8Z_ETIMEOUT);
             return false;
         }
     }
@@ -120,6 +140,13 @@ __device__ __forceinline__ void bulk_g2s_nohint(uint32_t dst, const void* src, u
         "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
         "l"(src), "r"(bytes), "r"(bar)
         : "memory");
+}
+
+// A tensor map kept in global memory and written there by a host copy must be
+// acquired into the tensor-map proxy before the copy engine uses it (system
+// scope: the writer was the host).  Once per map per thread is enough.
+__device__ __forceinline__ void tensormap_acquire(const void* map) {
+    asm volatile("fence.proxy.tensormap::generic.acquire.sys [%0], 128;" ::"l"(map) : "memory");
 }
 
 // Tiled 3-D tensor-map load into shared memory (x innermost; x * element size

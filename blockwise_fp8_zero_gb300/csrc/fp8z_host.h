@@ -21,9 +21,13 @@ struct NvtxRange {
     NvtxRange& operator=(const NvtxRange&) = delete;
 };
 
-// Limit for every bounded device wait (2 s): far above any legitimate wait in
-// a step, far below anything that would look like a hung GPU.
+// Default limit for every bounded device wait (2 s): far above any legitimate
+// wait in a step, far below anything that would look like a hung GPU.
 constexpr int64_t kDefaultTimeoutNs = 2000000000LL;
+
+// The limit the next launches take: kDefaultTimeoutNs unless
+// fp8z_set_wait_limit_ns changed it (process-wide).
+int64_t wait_limit_ns();
 
 inline bool aligned(const void* ptr, uintptr_t a) {
     return (reinterpret_cast<uintptr_t>(ptr) & (a - 1)) == 0;

@@ -70,6 +70,12 @@ int device_sms(int* sms) {
 }
 
 namespace {
+std::atomic<int64_t> g_wait_limit_ns{kDefaultTimeoutNs};
+}  // namespace
+
+int64_t wait_limit_ns() { return g_wait_limit_ns.load(std::memory_order_relaxed); }
+
+namespace {
 constexpr int kMaxDevices = 64;
 constexpr int kMaxSlots = 10;
 std::atomic<int> g_smem_done[kMaxSlots][kMaxDevices];
@@ -123,6 +129,15 @@ void* tensor_map_encoder() {
 
 }  // namespace host
 }  // namespace fp8z
+
+extern "C" int fp8z_set_wait_limit_ns(int64_t ns) {
+    if (ns < 0 || ns > 10000000000LL) return FP8Z_EINVAL;
+    fp8z::host::g_wait_limit_ns.store(ns == 0 ? fp8z::host::kDefaultTimeoutNs : ns,
+                                      std::memory_order_relaxed);
+    return FP8Z_OK;
+}
+
+extern "C" int64_t fp8z_get_wait_limit_ns(void) { return fp8z::host::wait_limit_ns(); }
 
 extern "C" const char* fp8z_status_string(int status) {
     switch (status) {

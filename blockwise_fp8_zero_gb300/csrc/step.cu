@@ -439,6 +439,7 @@ __global__ void __launch_bounds__(kThreads, 1) fp8z_step_kernel(const StepArgs A
         int slot = 0;
         uint32_t phase = 0;
         int64_t issued = 0;
+        int32_t acquired_map = -1;        // row-major: the grad map this thread last acquired
         BlockInfo pbi = load_desc(A, sched.blk(0));
         ctx[0].bi = pbi;
         ctx[0].pi = load_param(A, pbi);
@@ -453,6 +454,10 @@ __global__ void __launch_bounds__(kThreads, 1) fp8z_step_kernel(const StepArgs A
             // row-major grad: the stage is rows [k*16, k*16+16) of the block's
             // 128x128 tile of the param's [E,H,W] grad, zero past its edge
             const bool gmap_ok = kRowMajor && pbi.param >= 0 && pbi.param < A.nparams;
+            if (gmap_ok && pbi.param != acquired_map) {
+                tensormap_acquire(A.g_maps + pbi.param);
+                acquired_map = pbi.param;
+            }
             for (int k = 0; k < kStagesPerBlock; ++k) {
                 if (has_next && k == kStagesPerBlock / 2) pinext = load_param(A, pnext);
                 if (!mbar_wait_bounded(empty0 + 8 * slot, phase ^ 1, wd)) goto drain;
@@ -498,14 +503,16 @@ __global__ void __launch_bounds__(kThreads, 1) fp8z_step_kernel(const StepArgs A
             }
             pbi = pnext;
         }
-        return;
     drain:
-        // Abort: let the copies already issued land before the CTA exits.
-        for (int64_t j = (issued > kRing ? issued - kRing : 0); j < issued; ++j) {
-            const int s = int(j % kRing);
-            const uint32_t ph = uint32_t((j / kRing) & 1);
-            mbar_wait_bounded(full0 + 8 * s, ph, wd, /*honor_abort=*/false);
-        }
+        // After the last stage, or after giving up: every copy this thread
+        // issued lands before it leaves, so the CTA never exits (consumers
+        // that gave up may already have left) while the copy engine still
+        // writes its ring.  Only the last kRing stages can be in flight: each
+        // earlier stage shared its slot with a later one, issued only after
+        // the consumers had read it.  The drain wait ignores the abort flag and
+        // has its own, far longer limit.
+        for (int64_t j = (issued > kRing ? issued - kRing : 0); j < issued; ++j)
+            mbar_wait_drain(full0 + 8 * int(j % kRing), uint32_t((j / kRing) & 1), A.dev_status);
         return;
     }
 
@@ -695,7 +702,7 @@ int prepare(StepArgs& A, float* p, float* m, float* v, int64_t capacity_blocks,
     A.inv_scale_t = want_t ? inv_scale_t : nullptr;
     A.inv_scale_t_count = inv_scale_t_count;
     A.dev_status = dev_status;
-    A.timeout_ns = host::kDefaultTimeoutNs;
+    A.timeout_ns = host::wait_limit_ns();
     const host::AdamwScalars sc = host::adamw_scalars(*hp);
     A.beta1 = sc.beta1; A.beta2 = sc.beta2; A.omb1 = sc.omb1; A.omb2 = sc.omb2;
     A.eps = sc.eps; A.step_size = sc.step_size; A.rs_bc2 = sc.rs_bc2;

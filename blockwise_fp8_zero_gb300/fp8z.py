@@ -48,7 +48,8 @@ EXPORTED = ("fp8z_plan_shards", "fp8z_adamw_requant_step", "fp8z_adamw_requant_s
             "fp8z_encode_grad_maps", "fp8z_dequant",
             "fp8z_transpose_fp8", "fp8z_fold", "fp8z_unfold", "fp8z_quantize_rowwise",
             "fp8z_transpose_rowwise", "fp8z_e4m3_encode_bits",
-            "fp8z_watchdog_selftest", "fp8z_status_string")
+            "fp8z_watchdog_selftest", "fp8z_set_wait_limit_ns", "fp8z_get_wait_limit_ns",
+            "fp8z_status_string")
 
 
 class fp8z_adamw_hparams(ctypes.Structure):
@@ -106,11 +107,14 @@ def lib():
         L.fp8z_transpose_rowwise.argtypes = [P, P, i64, i64, P, P, P]
         L.fp8z_e4m3_encode_bits.argtypes = [ctypes.c_uint32, i64, P, P]
         L.fp8z_watchdog_selftest.argtypes = [P, i64, P]
+        L.fp8z_set_wait_limit_ns.argtypes = [i64]
+        L.fp8z_get_wait_limit_ns.argtypes = []
         L.fp8z_status_string.argtypes = [ctypes.c_int]
         L.fp8z_status_string.restype = ctypes.c_char_p
         for name in EXPORTED:
             if name != "fp8z_status_string":
                 getattr(L, name).restype = ctypes.c_int
+        L.fp8z_get_wait_limit_ns.restype = i64
         _lib = L
     return _lib
 
@@ -139,6 +143,22 @@ def _dptr(t, dtype=None, name="tensor"):
     if t.device.index is not None and t.device.index != cur:
         raise ValueError(f"{name} is on {t.device}, but the current device is cuda:{cur}")
     return t.data_ptr()
+
+
+DESC_BYTES = block_desc_dtype.itemsize       # 20
+ENTRY_BYTES = param_entry_dtype.itemsize     # 64
+
+
+def _check_tables(cap, desc, params, nparams):
+    """The kernels read desc[b] for every block b < capacity and params[i] for
+    i < nparams: a shorter table would be read past its end on the device, so
+    it is refused here, before any launch."""
+    if desc is not None and desc.numel() * desc.element_size() < cap * DESC_BYTES:
+        raise ValueError(f"desc holds {desc.numel() * desc.element_size()} bytes, "
+                         f"{cap} blocks need {cap * DESC_BYTES}")
+    if params is not None and params.numel() * params.element_size() < int(nparams) * ENTRY_BYTES:
+        raise ValueError(f"params holds {params.numel() * params.element_size()} bytes, "
+                         f"{int(nparams)} entries need {int(nparams) * ENTRY_BYTES}")
 
 
 def _stream_handle(stream):
@@ -200,6 +220,7 @@ def fp8z_adamw_requant_step(p, g, m, v, w_fp8, inv_scale, blk_begin, nblk, hp,
             raise ValueError(f"{name} must have as many elements as p")
     if inv_scale.numel() < cap:
         raise ValueError("inv_scale must hold one scale per block")
+    _check_tables(cap, desc, params, nparams)
     rc = lib().fp8z_adamw_requant_step(
         _dptr(p, torch.float32, "p"), _dptr(g, torch.float32, "g"),
         _dptr(m, torch.float32, "m"), _dptr(v, torch.float32, "v"),
@@ -224,6 +245,7 @@ def fp8z_adamw_requant_step_mx(p, g, m, v, w_fp8, mx_scale, blk_begin, nblk, hp,
             raise ValueError(f"{name} must have as many elements as p")
     if mx_scale.numel() < cap * (BLOCK_ELEMS // 32):
         raise ValueError("mx_scale must hold 512 bytes per block")
+    _check_tables(cap, desc, None, 0)
     rc = lib().fp8z_adamw_requant_step_mx(
         _dptr(p, torch.float32, "p"), _dptr(g, torch.float32, "g"), _dptr(m, torch.float32, "m"),
         _dptr(v, torch.float32, "v"), _dptr(w_fp8, torch.uint8, "w_fp8"),
@@ -268,6 +290,9 @@ def fp8z_adamw_requant_step_rowmajor(p, m, v, g_maps, w_row, inv_scale, blk_begi
         raise ValueError("inv_scale must hold one scale per block")
     if g_maps.numel() < nparams * 128:
         raise ValueError("g_maps must hold one 128-byte map per param")
+    if desc is None or params is None:
+        raise ValueError("the row-major step needs desc and params")
+    _check_tables(cap, desc, params, nparams)
     rc = lib().fp8z_adamw_requant_step_rowmajor(
         _dptr(p, torch.float32, "p"), _dptr(m, torch.float32, "m"), _dptr(v, torch.float32, "v"),
         _dptr(g_maps, torch.uint8, "g_maps"), _dptr(w_row, torch.uint8, "w_row"), w_row.numel(),
@@ -302,6 +327,8 @@ def fp8z_transpose_fp8(w_fp8, inv_scale, entry, out, inv_scale_t, dev_status=Non
         raise ValueError("output buffers too small")
     if w_fp8.numel() < (int(entry["blk_offset"]) + nb) * BLOCK_ELEMS:
         raise ValueError("w_fp8 does not hold the param's blocks")
+    if inv_scale.numel() < int(entry["blk_offset"]) + nb:
+        raise ValueError("inv_scale does not hold the param's scales")
     rc = lib().fp8z_transpose_fp8(_dptr(w_fp8, torch.uint8, "w_fp8"),
                                   _dptr(inv_scale, torch.float32, "inv_scale"), ent.ctypes.data,
                                   _dptr(out, torch.uint8, "out"),
@@ -381,3 +408,12 @@ def fp8z_watchdog_selftest(dev_status, timeout_ns, stream=None):
     rc = lib().fp8z_watchdog_selftest(_dptr(dev_status, torch.int32, "dev_status"),
                                       int(timeout_ns), _stream_handle(stream))
     _check("fp8z_watchdog_selftest", rc)
+
+
+def fp8z_set_wait_limit_ns(ns):
+    """Limit (ns) of every bounded device wait in later launches; 0 restores 2 s."""
+    _check("fp8z_set_wait_limit_ns", lib().fp8z_set_wait_limit_ns(int(ns)))
+
+
+def fp8z_get_wait_limit_ns():
+    return int(lib().fp8z_get_wait_limit_ns())

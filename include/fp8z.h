@@ -355,6 +355,21 @@ FP8Z_API int fp8z_e4m3_encode_bits(uint32_t first_bits, int64_t n, uint8_t *out,
  */
 FP8Z_API int fp8z_watchdog_selftest(int32_t *dev_status, int64_t timeout_ns, void *stream);
 
+/*
+ * fp8z_set_wait_limit_ns / fp8z_get_wait_limit_ns -- the time limit of every
+ * bounded device wait (the barrier waits of the step, dequant, transpose and
+ * fold kernels) in launches enqueued after the call.  Process-wide, host only,
+ * thread-safe.  ns = 0 restores the default of 2 s; 1 .. 10^10 sets the limit;
+ * anything else is FP8Z_EINVAL.  When a wait reaches the limit its kernel
+ * writes FP8Z_ETIMEOUT to *dev_status, lets the copies it has in flight land
+ * (with a separate limit of 20 s that this setting does not change) and
+ * returns; the outputs of that launch are then incomplete.  A very short
+ * limit exists to exercise that path in tests and diagnostics; the default
+ * is far above any wait of a working launch.
+ */
+FP8Z_API int fp8z_set_wait_limit_ns(int64_t ns);
+FP8Z_API int64_t fp8z_get_wait_limit_ns(void);
+
 /* Static string naming a status code (never NULL). */
 FP8Z_API const char *fp8z_status_string(int status);
 

@@ -182,3 +182,56 @@ def test_rowwise_and_mx_argument_errors(L):
     bad = fp8z.hparams()
     bad.eps = 0.0
     assert mx(hp=bad) == fp8z.FP8Z_EINVAL
+
+
+def test_wait_limit_knob(L):
+    """The process-wide limit of the bounded device waits: host only, checked
+    range, 0 restores the 2 s default."""
+    default = 2_000_000_000
+    assert fp8z.fp8z_get_wait_limit_ns() == default
+    try:
+        fp8z.fp8z_set_wait_limit_ns(300)
+        assert fp8z.fp8z_get_wait_limit_ns() == 300
+        assert L.fp8z_set_wait_limit_ns(-1) == fp8z.FP8Z_EINVAL
+        assert L.fp8z_set_wait_limit_ns(10 ** 10 + 1) == fp8z.FP8Z_EINVAL
+        assert fp8z.fp8z_get_wait_limit_ns() == 300            # a refused value changes nothing
+        fp8z.fp8z_set_wait_limit_ns(10 ** 10)
+        assert fp8z.fp8z_get_wait_limit_ns() == 10 ** 10
+    finally:
+        fp8z.fp8z_set_wait_limit_ns(0)
+    assert fp8z.fp8z_get_wait_limit_ns() == default
+
+
+def test_bindings_refuse_short_tables():
+    """A descriptor or param table shorter than the launch reads is refused by
+    the binding before any pointer is taken (CPU tensors: the size check comes
+    first, so no device is needed)."""
+    torch = pytest.importorskip("torch")
+    cap = 4
+    f = lambda n, dt=torch.float32: torch.zeros(n, dtype=dt)
+    p, g, m, v = (f(cap * fp8z.BLOCK_ELEMS) for _ in range(4))
+    q = f(cap * fp8z.BLOCK_ELEMS, torch.uint8)
+    inv = f(cap)
+    hp = fp8z.hparams()
+    short_desc = f(cap * 20 - 1, torch.uint8)
+    with pytest.raises(ValueError, match="desc"):
+        fp8z.fp8z_adamw_requant_step(p, g, m, v, q, inv, 0, 1, hp, desc=short_desc)
+    with pytest.raises(ValueError, match="params"):
+        fp8z.fp8z_adamw_requant_step(p, g, m, v, q, inv, 0, 1, hp, desc=f(cap * 20, torch.uint8),
+                                     params=f(64 * 2 - 1, torch.uint8), nparams=2,
+                                     w_fp8_t=f(16, torch.uint8), inv_scale_t=f(4))
+    with pytest.raises(ValueError, match="desc"):
+        fp8z.fp8z_adamw_requant_step_mx(p, g, m, v, q, f(cap * 512, torch.uint8), 0, 1, hp,
+                                        desc=short_desc)
+    maps = f(128, torch.uint8)
+    with pytest.raises(ValueError, match="desc"):
+        fp8z.fp8z_adamw_requant_step_rowmajor(p, m, v, maps, f(16, torch.uint8), inv, 0, 1, hp,
+                                              short_desc, f(64, torch.uint8), 1)
+    with pytest.raises(ValueError, match="params"):
+        fp8z.fp8z_adamw_requant_step_rowmajor(p, m, v, maps, f(16, torch.uint8), inv, 0, 1, hp,
+                                              f(cap * 20, torch.uint8), f(63, torch.uint8), 1)
+    ent = np.zeros(1, fp8z.param_entry_dtype)
+    ent[0] = (2, 0, 0, 1, 128, 128, 1, 1, 0, 0)                  # blocks 2 .. 2 of a 3-block buffer
+    with pytest.raises(ValueError, match="inv_scale"):
+        fp8z.fp8z_transpose_fp8(f(3 * fp8z.BLOCK_ELEMS, torch.uint8), f(2), ent[0],
+                                f(128 * 128, torch.uint8), f(1))
