@@ -28,6 +28,7 @@
 // param's [E,H,W] tensor, E4M3 written row-major: the fold/unfold fused in);
 // and the MXFP8 variant (an E8M0 scale per 32 elements, cast stage by stage
 // with no block-wide amax).
+#include <atomic>
 #include <cfloat>
 #include <cmath>
 #include <cstdint>
@@ -825,4 +826,75 @@ extern "C" int fp8z_encode_grad_maps(const void* const* g_ptrs, const fp8z_param
             return FP8Z_EINVAL;
     }
     return FP8Z_OK;
+}
+
+// ------------------------------------------- row-major step, no allocation
+// The grad tensor maps of fp8z_adamw_requant_step_rowmajor_static live in this
+// array, not in a buffer the caller allocates.  Every device that loads the
+// library holds it (128 KB) until the process exits; host code reaches it
+// only through the address cudaGetSymbolAddress gives for the current device.
+static __device__ __align__(256) CUtensorMap g_static_grad_maps[FP8Z_STATIC_GRAD_MAPS];
+
+namespace {
+
+constexpr int kMaxStaticDevices = 64;
+std::atomic<void*> g_static_maps_addr[kMaxStaticDevices];
+
+// Device address of g_static_grad_maps on the current device, looked up once
+// per device (with that device current) and kept.
+int static_maps_address(void** addr) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return FP8Z_ECUDA;
+    if (dev < 0 || dev >= kMaxStaticDevices) return FP8Z_EUNSUPPORTED;
+    void* a = g_static_maps_addr[dev].load(std::memory_order_acquire);
+    if (!a) {
+        if (cudaGetSymbolAddress(&a, g_static_grad_maps) != cudaSuccess || !a) return FP8Z_ECUDA;
+        g_static_maps_addr[dev].store(a, std::memory_order_release);
+    }
+    *addr = a;
+    return FP8Z_OK;
+}
+
+}  // namespace
+
+extern "C" int fp8z_adamw_requant_step_rowmajor_static(
+    float* p, float* m, float* v, const void* const* g_ptrs, const fp8z_param_entry* params_host,
+    uint8_t* w_row, int64_t w_row_bytes, float* inv_scale, int64_t capacity_blocks, int64_t blk_begin,
+    int64_t nblk, const fp8z_block_desc* desc, const fp8z_param_entry* params, int32_t nparams,
+    uint8_t* w_fp8_t, int64_t w_fp8_t_bytes, float* inv_scale_t, int64_t inv_scale_t_count,
+    const fp8z_adamw_hparams* hp, int32_t* dev_status, void* stream) {
+    const fp8z::host::NvtxRange nvtx_range("fp8z_adamw_requant_step_rowmajor_static");
+    if (!g_ptrs || !params_host || !w_row || !inv_scale || !desc || !params || nparams <= 0 ||
+        w_row_bytes < 0)
+        return FP8Z_EINVAL;
+    if (nparams > FP8Z_STATIC_GRAD_MAPS) return FP8Z_ENOSPACE;
+    if (!host::aligned(w_row, 16) || !host::aligned(inv_scale, 4)) return FP8Z_EALIGN;
+    StepArgs A;
+    int rc = prepare(A, p, m, v, capacity_blocks, blk_begin, nblk, desc, params, nparams, w_fp8_t,
+                     w_fp8_t_bytes, inv_scale_t, inv_scale_t_count, hp, dev_status);
+    if (rc != FP8Z_OK) return rc;
+    if (nblk == 0) return FP8Z_OK;
+    void* maps = nullptr;
+    rc = static_maps_address(&maps);
+    if (rc != FP8Z_OK) return rc;
+    // Encode the maps on the host a few at a time and copy them into the
+    // array on the stream, ahead of the launch.  A copy from pageable host
+    // memory has read its source by the time cudaMemcpyAsync returns, so the
+    // staging buffer can be reused at once.
+    constexpr int kChunk = 32;
+    alignas(64) CUtensorMap chunk[kChunk];
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    for (int32_t i = 0; i < nparams; i += kChunk) {
+        const int32_t n = nparams - i < kChunk ? nparams - i : kChunk;
+        rc = fp8z_encode_grad_maps(g_ptrs + i, params_host + i, n, chunk);
+        if (rc != FP8Z_OK) return rc;
+        if (cudaMemcpyAsync(static_cast<CUtensorMap*>(maps) + i, chunk, size_t(n) * sizeof(CUtensorMap),
+                            cudaMemcpyHostToDevice, st) != cudaSuccess)
+            return FP8Z_ECUDA;
+    }
+    A.g_maps = static_cast<const CUtensorMap*>(maps);
+    A.inv_scale = inv_scale;
+    A.w_row = w_row;
+    A.w_row_bytes = w_row_bytes;
+    return launch<true, false>(A, stream);
 }

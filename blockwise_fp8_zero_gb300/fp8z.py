@@ -44,7 +44,7 @@ plan_summary_dtype = np.dtype([
 assert param_entry_dtype.itemsize == 64 and block_desc_dtype.itemsize == 20
 
 EXPORTED = ("fp8z_plan_shards", "fp8z_adamw_requant_step", "fp8z_adamw_requant_step_rowmajor",
-            "fp8z_adamw_requant_step_mx",
+            "fp8z_adamw_requant_step_mx", "fp8z_adamw_requant_step_rowmajor_static",
             "fp8z_encode_grad_maps", "fp8z_dequant",
             "fp8z_transpose_fp8", "fp8z_fold", "fp8z_unfold", "fp8z_quantize_rowwise",
             "fp8z_transpose_rowwise", "fp8z_e4m3_encode_bits",
@@ -97,6 +97,9 @@ def lib():
                                                        P, i64, P, i64,
                                                        ctypes.POINTER(fp8z_adamw_hparams), P, P]
         L.fp8z_encode_grad_maps.argtypes = [P, P, i32, P]
+        L.fp8z_adamw_requant_step_rowmajor_static.argtypes = [P, P, P, P, P, P, i64, P, i64, i64, i64, P,
+                                                              P, i32, P, i64, P, i64,
+                                                              ctypes.POINTER(fp8z_adamw_hparams), P, P]
         L.fp8z_adamw_requant_step_mx.argtypes = [P, P, P, P, P, P, i64, i64, i64, P,
                                                  ctypes.POINTER(fp8z_adamw_hparams), P, P]
         L.fp8z_dequant.argtypes = [P, P, i64, P, P, P]
@@ -303,6 +306,42 @@ def fp8z_adamw_requant_step_rowmajor(p, m, v, g_maps, w_row, inv_scale, blk_begi
         0 if inv_scale_t is None else inv_scale_t.numel(),
         ctypes.byref(hp), _dptr(dev_status, torch.int32, "dev_status"), _stream_handle(stream))
     _check("fp8z_adamw_requant_step_rowmajor", rc)
+
+
+def fp8z_adamw_requant_step_rowmajor_static(p, m, v, grads, params_host, w_row, inv_scale, blk_begin,
+                                            nblk, hp, desc, params, nparams, w_fp8_t=None,
+                                            inv_scale_t=None, dev_status=None, stream=None):
+    """The row-major step for callers that cannot allocate device memory: the
+    grad tensor maps go into an array inside the library instead of a
+    caller-allocated g_maps buffer.  grads: one row-major float32 CUDA tensor
+    per param; params_host: the planner's param table (numpy, host)."""
+    import torch
+    cap = p.numel() // BLOCK_ELEMS
+    for t, name in ((m, "m"), (v, "v")):
+        if t.numel() != p.numel():
+            raise ValueError(f"{name} must have as many elements as p")
+    if inv_scale.numel() < cap:
+        raise ValueError("inv_scale must hold one scale per block")
+    if desc is None or params is None:
+        raise ValueError("the row-major step needs desc and params")
+    _check_tables(cap, desc, params, nparams)
+    ent = np.ascontiguousarray(params_host, dtype=param_entry_dtype)
+    if len(grads) != int(nparams) or len(ent) != int(nparams):
+        raise ValueError("one grad and one host param entry per param")
+    for gt, pe in zip(grads, ent):
+        if gt.dtype != torch.float32 or gt.numel() < int(pe["e"]) * int(pe["rows"]) * int(pe["cols"]):
+            raise ValueError("grad must be float32 and hold the whole param")
+    ptrs = (ctypes.c_void_p * len(grads))(*[_dptr(gt, torch.float32, "grad") for gt in grads])
+    rc = lib().fp8z_adamw_requant_step_rowmajor_static(
+        _dptr(p, torch.float32, "p"), _dptr(m, torch.float32, "m"), _dptr(v, torch.float32, "v"),
+        ptrs, ent.ctypes.data, _dptr(w_row, torch.uint8, "w_row"), w_row.numel(),
+        _dptr(inv_scale, torch.float32, "inv_scale"), cap, int(blk_begin), int(nblk),
+        _dptr(desc, torch.uint8, "desc"), _dptr(params, torch.uint8, "params"), int(nparams),
+        _dptr(w_fp8_t, torch.uint8, "w_fp8_t"), 0 if w_fp8_t is None else w_fp8_t.numel(),
+        _dptr(inv_scale_t, torch.float32, "inv_scale_t"),
+        0 if inv_scale_t is None else inv_scale_t.numel(),
+        ctypes.byref(hp), _dptr(dev_status, torch.int32, "dev_status"), _stream_handle(stream))
+    _check("fp8z_adamw_requant_step_rowmajor_static", rc)
 
 
 def fp8z_dequant(w_fp8, inv_scale, nblk, out, dev_status=None, stream=None):

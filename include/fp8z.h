@@ -222,6 +222,46 @@ FP8Z_API int fp8z_adamw_requant_step_rowmajor(float *p, float *m, float *v, cons
                                               void *stream);
 
 /*
+ * fp8z_adamw_requant_step_rowmajor_static -- fp8z_adamw_requant_step_rowmajor
+ * for callers that cannot allocate device memory.  The pages have no
+ * counterpart: this is a service of the library, not a step of the method.
+ *
+ * Some callers cannot call cudaMalloc where the step runs: code inside another
+ * framework's training step that may only use the tensors that framework hands
+ * it, a caller that must not stall the device (an allocation can synchronize
+ * it), or one whose device memory is already committed to the optimizer
+ * state.  The row-major step needs one piece of working memory besides its
+ * inputs and outputs: the grad tensor maps (128 bytes per param) that
+ * fp8z_adamw_requant_step_rowmajor reads from a caller-allocated g_maps
+ * buffer.  This entry point keeps them instead in an array inside the library
+ * (FP8Z_STATIC_GRAD_MAPS maps, 128 KB, held on every device that loads the
+ * library until the process exits), so it allocates nothing.
+ *
+ * g_ptrs: HOST array of nparams device pointers, param i's row-major FP32 grad
+ *   [e, rows, cols] (rules as for fp8z_encode_grad_maps).
+ * params_host: HOST copy of the planner's param table (the same entries as the
+ *   device table `params`); the maps are encoded from it on the host and
+ *   copied into the library's array on `stream` before the launch.
+ * Every other argument, the arithmetic and the results are exactly those of
+ * fp8z_adamw_requant_step_rowmajor.
+ * nparams > FP8Z_STATIC_GRAD_MAPS is refused with FP8Z_ENOSPACE, before any
+ * device work.  The first call on a device looks up the array's device
+ * address (cudaGetSymbolAddress, with that device current) and keeps it;
+ * make that first call before any stream capture.  Every call shares the one
+ * array per device: calls whose work overlaps on the GPU (for instance on two
+ * streams) race on it, so issue them in one stream or order them.  The array
+ * keeps the maps of the last call.  Calls neither cudaMalloc nor cudaFree nor
+ * any routine that allocates device memory.
+ */
+#define FP8Z_STATIC_GRAD_MAPS 1024
+FP8Z_API int fp8z_adamw_requant_step_rowmajor_static(
+    float *p, float *m, float *v, const void *const *g_ptrs, const fp8z_param_entry *params_host,
+    uint8_t *w_row, int64_t w_row_bytes, float *inv_scale, int64_t capacity_blocks, int64_t blk_begin,
+    int64_t nblk, const fp8z_block_desc *desc, const fp8z_param_entry *params, int32_t nparams,
+    uint8_t *w_fp8_t, int64_t w_fp8_t_bytes, float *inv_scale_t, int64_t inv_scale_t_count,
+    const fp8z_adamw_hparams *hp, int32_t *dev_status, void *stream);
+
+/*
  * fp8z_adamw_requant_step_mx -- the step with an MXFP8 output instead of the
  * 128x128 block scales: E4M3 codes with one E8M0 power-of-two scale per 32
  * consecutive elements of a block row.  "A ZeRO Optimizer Design for Blockwise
