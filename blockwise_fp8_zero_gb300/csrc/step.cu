@@ -98,7 +98,7 @@ constexpr size_t kRingBytes = size_t(kRing) * kStageBytes;
 constexpr size_t kTileBytes = kBlkElems;                 // 16 KB byte tile
 constexpr size_t kAmaxBytes = 2 * kConsumerWarps * sizeof(float);
 constexpr size_t kCtxOffset = kRingBytes + kTileBytes + kAmaxBytes;
-constexpr size_t kCtxBytes = 2 * 80;                     // two BlockCtx slots
+constexpr size_t kCtxBytes = 2 * 96;                     // two BlockCtx slots
 constexpr size_t kBarOffset = kCtxOffset + kCtxBytes;
 constexpr int kNumBars = 2 * kRing + 2;
 constexpr size_t kSmemBytes = kBarOffset + kNumBars * 8 + 16;
@@ -222,6 +222,27 @@ struct ParamInfo {
     int64_t e, H, W, hb, wb, t_off, ts_off;
 };
 
+// Row-major variant: how a block's grad reaches the consumers.
+enum GradMode : int32_t {
+    kGradZero = 0,       // no valid grad (bad descriptor or map slot): grad 0
+    kGradTma = 1,        // a tensor-map load into the ring's grad section
+    kGradPlain = 2,      // plain loads from the param's row-major grad
+};
+
+// A row-major grad whose row pitch is not a multiple of 16 bytes cannot be
+// described by a tensor map (a TMA rule); its 128-byte slot in the map table
+// holds this record instead, and the consumers read that grad with plain
+// 4-byte loads.  The kernel tells the two apart by the param's column count
+// (cols % 4 != 0: a record) and checks the record's tag and shape.
+struct PlainGrad {
+    uint64_t magic;          // kPlainGradMagic
+    const float* ptr;        // the grad [e, rows, cols], 4-byte aligned
+    int64_t e, rows, cols;   // its shape, equal to the param entry's
+    uint64_t pad[11];
+};
+static_assert(sizeof(PlainGrad) == 128, "one map slot");
+constexpr uint64_t kPlainGradMagic = 0x31647267506e6c70ull;
+
 // A block's descriptor and param entry, fetched from global memory by the
 // producer one block ahead and handed to the consumers through shared memory
 // (written before the block's first stage is armed; the mbarrier's
@@ -231,8 +252,11 @@ struct ParamInfo {
 struct BlockCtx {
     BlockInfo bi;        // 24 bytes
     ParamInfo pi;        // 56 bytes
+    const float* g_rows; // row-major, kGradPlain: base of the param's grad
+    int32_t g_mode;      // row-major: GradMode of the block
+    int32_t pad;
 };
-static_assert(sizeof(BlockCtx) == 80, "context slot size");
+static_assert(sizeof(BlockCtx) == 96, "context slot size");
 static_assert(kRing <= kStagesPerBlock, "context slots need the producer within one block");
 // the deferred column-major copy reads the previous block's context slot
 // before releasing stage 1; the producer refills that slot once stage
@@ -294,18 +318,59 @@ __device__ __forceinline__ BlockSched block_sched(int64_t blk_begin, int64_t nbl
                       (nblk - blockIdx.x + gridDim.x - 1) / gridDim.x};
 }
 
+// Does descriptor bi name a block of param pi: index, expert, block position
+// and ragged edge all agreeing with the param table?
+__device__ __forceinline__ bool block_in_param(const StepArgs& A, const BlockInfo& bi, const ParamInfo& pi) {
+    return bi.param >= 0 && bi.param < A.nparams && bi.e >= 0 && bi.e < pi.e && bi.brow >= 0 &&
+           bi.brow < pi.hb && bi.bcol >= 0 && bi.bcol < pi.wb &&
+           bi.vr == imin64(kBlk, pi.H - bi.brow * int64_t(kBlk)) &&
+           bi.vc == imin64(kBlk, pi.W - bi.bcol * int64_t(kBlk));
+}
+
 // Does block bi of param pi have a destination inside a buffer of `bytes`
 // bytes (and, for the transposed grid, `scales` entries)?  A descriptor that
 // disagrees with the param table is rejected, so no write can leave the buffer.
 __device__ __forceinline__ bool dest_ok(const StepArgs& A, const BlockInfo& bi, const ParamInfo& pi,
                                         int64_t bytes, int64_t scales) {
     const int64_t H = pi.H, W = pi.W;
-    return bi.param >= 0 && bi.param < A.nparams && bi.e >= 0 && bi.e < pi.e && bi.brow >= 0 &&
-           bi.brow < pi.hb && bi.bcol >= 0 && bi.bcol < pi.wb &&
-           bi.vr == imin64(kBlk, H - bi.brow * int64_t(kBlk)) &&
-           bi.vc == imin64(kBlk, W - bi.bcol * int64_t(kBlk)) && pi.t_off >= 0 &&
-           pi.t_off + (bi.e + 1) * H * W <= bytes &&
+    return block_in_param(A, bi, pi) && pi.t_off >= 0 && pi.t_off + (bi.e + 1) * H * W <= bytes &&
            (scales < 0 || (pi.ts_off >= 0 && pi.ts_off + (bi.e + 1) * pi.hb * pi.wb <= scales));
+}
+
+// Row-major variant: how block bi's grad is read, from its param's slot in the
+// map table.  A slot that does not match the param entry (a record where a
+// tensor map belongs, or a record with another shape) gives kGradZero and
+// FP8Z_EINVAL; plain loads also need the descriptor to agree with the param
+// table, since they are not clipped at the tensor's edge like a TMA load.
+__device__ __forceinline__ int32_t grad_mode(const StepArgs& A, const BlockInfo& bi, const ParamInfo& pi,
+                                             const float*& g_rows) {
+    g_rows = nullptr;
+    if (bi.param < 0 || bi.param >= A.nparams) return kGradZero;
+    const PlainGrad* r = reinterpret_cast<const PlainGrad*>(A.g_maps + bi.param);
+    const bool record = r->magic == kPlainGradMagic;
+    if ((pi.W & 3) == 0) {
+        if (!record) return kGradTma;
+    } else if (record && block_in_param(A, bi, pi) && r->e == pi.e && r->rows == pi.H && r->cols == pi.W) {
+        g_rows = r->ptr;
+        return kGradPlain;
+    }
+    report_status(A.dev_status, FP8Z_EINVAL);
+    return kGradZero;
+}
+
+// Row-major variant, kGradPlain: the four grad values of (block row `row`,
+// columns col..col+3) of block bi, zero past the ragged edge.
+__device__ __forceinline__ float4 load_grad_plain(const float* g_rows, const BlockInfo& bi, int64_t H, int64_t W,
+                                                  int row, int col) {
+    float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (row >= bi.vr) return x;
+    const float* src =
+        g_rows + (int64_t(bi.e) * H + int64_t(bi.brow) * kBlk + row) * W + int64_t(bi.bcol) * kBlk + col;
+    if (col + 0 < bi.vc) x.x = __ldg(src + 0);
+    if (col + 1 < bi.vc) x.y = __ldg(src + 1);
+    if (col + 2 < bi.vc) x.z = __ldg(src + 2);
+    if (col + 3 < bi.vc) x.w = __ldg(src + 3);
+    return x;
 }
 
 // Row-major E4M3 write of one block into the whole-param buffer ("Summary"
@@ -442,8 +507,16 @@ __global__ void __launch_bounds__(kThreads, 1) fp8z_step_kernel(const StepArgs A
         int64_t issued = 0;
         int32_t acquired_map = -1;        // row-major: the grad map this thread last acquired
         BlockInfo pbi = load_desc(A, sched.blk(0));
-        ctx[0].bi = pbi;
-        ctx[0].pi = load_param(A, pbi);
+        int32_t pmode = kGradZero;
+        {
+            const ParamInfo pi0 = load_param(A, pbi);
+            const float* g_rows = nullptr;
+            if (kRowMajor) pmode = grad_mode(A, pbi, pi0, g_rows);
+            ctx[0].bi = pbi;
+            ctx[0].pi = pi0;
+            ctx[0].g_rows = g_rows;
+            ctx[0].g_mode = pmode;
+        }
         for (int64_t i = 0; i < nmine; ++i) {
             const size_t base = size_t(sched.blk(i)) * kBlkElems;
             const bool has_next = i + 1 < nmine;
@@ -452,10 +525,11 @@ __global__ void __launch_bounds__(kThreads, 1) fp8z_step_kernel(const StepArgs A
             BlockInfo pnext = pbi;
             ParamInfo pinext{0, 0, 0, 0, 0, 0, 0};
             if (has_next) pnext = load_desc(A, sched.blk(i + 1));
-            // row-major grad: the stage is rows [k*16, k*16+16) of the block's
-            // 128x128 tile of the param's [E,H,W] grad, zero past its edge
-            const bool gmap_ok = kRowMajor && pbi.param >= 0 && pbi.param < A.nparams;
-            if (gmap_ok && pbi.param != acquired_map) {
+            // row-major grad, kGradTma: the stage is rows [k*16, k*16+16) of
+            // the block's 128x128 tile of the param's [E,H,W] grad, zero past
+            // its edge; the other modes leave the ring's grad section unloaded
+            const bool g_tma = kRowMajor && pmode == kGradTma;
+            if (g_tma && pbi.param != acquired_map) {
                 tensormap_acquire(A.g_maps + pbi.param);
                 acquired_map = pbi.param;
             }
@@ -472,11 +546,11 @@ __global__ void __launch_bounds__(kThreads, 1) fp8z_step_kernel(const StepArgs A
                 // did, and this one costs no measurable time.
                 fence_proxy_async();
                 const uint32_t full = full0 + 8 * slot;
-                mbar_arrive_expect_tx(full, (kRowMajor && !gmap_ok) ? 3 * kTensorStageBytes : kStageBytes);
+                mbar_arrive_expect_tx(full, (kRowMajor && !g_tma) ? 3 * kTensorStageBytes : kStageBytes);
                 const uint32_t dst = ring0 + slot * kStageBytes;
                 const size_t off = base + size_t(k) * kStageElems;
                 if (kRowMajor) {
-                    if (gmap_ok)
+                    if (g_tma)
                         tma_load_3d(dst, A.g_maps + pbi.param, pbi.bcol * kBlk,
                                     pbi.brow * kBlk + k * kStageRows, pbi.e, full);
                 } else {
@@ -499,8 +573,12 @@ __global__ void __launch_bounds__(kThreads, 1) fp8z_step_kernel(const StepArgs A
                 if (++slot == kRing) { slot = 0; phase ^= 1; }
             }
             if (has_next) {
+                const float* g_rows = nullptr;
+                if (kRowMajor) pmode = grad_mode(A, pnext, pinext, g_rows);
                 ctx[(i + 1) & 1].bi = pnext;
                 ctx[(i + 1) & 1].pi = pinext;
+                ctx[(i + 1) & 1].g_rows = g_rows;
+                ctx[(i + 1) & 1].g_mode = pmode;
             }
             pbi = pnext;
         }
@@ -533,7 +611,10 @@ __global__ void __launch_bounds__(kThreads, 1) fp8z_step_kernel(const StepArgs A
         const size_t base = size_t(blk) * kBlkElems;
         const BlockCtx* c = ctx + (i & 1);
         int vr = kBlk, vc = kBlk;
-        bool g_ok = true;
+        int32_t g_mode = kGradTma;
+        const float* g_rows = nullptr;
+        BlockInfo gbi{};
+        int64_t gH = 0, gW = 0;
 
         float4 keep[kKeep];
         float lmax = 0.0f;
@@ -543,7 +624,15 @@ __global__ void __launch_bounds__(kThreads, 1) fp8z_step_kernel(const StepArgs A
             if (k == 0) {        // the block's context is visible once its first stage is
                 vr = c->bi.vr;
                 vc = c->bi.vc;
-                g_ok = !kRowMajor || (c->bi.param >= 0 && c->bi.param < A.nparams);
+                if (kRowMajor) {
+                    g_mode = c->g_mode;
+                    if (g_mode == kGradPlain) {
+                        g_rows = c->g_rows;
+                        gbi = c->bi;
+                        gH = c->pi.H;
+                        gW = c->pi.W;
+                    }
+                }
             }
             const float* st = ring + size_t(slot) * (kStageBytes / 4);
             float4 g4[kRowsPerWarp], p4[kRowsPerWarp], m4[kRowsPerWarp], v4[kRowsPerWarp];
@@ -558,9 +647,13 @@ __global__ void __launch_bounds__(kThreads, 1) fp8z_step_kernel(const StepArgs A
             __syncwarp();
             if (lane == 0) mbar_arrive(empty0 + 8 * slot);
             if (++slot == kRing) { slot = 0; phase ^= 1; }
-            if (kRowMajor && !g_ok) {
+            if (kRowMajor && g_mode != kGradTma) {
 #pragma unroll
-                for (int r = 0; r < kRowsPerWarp; ++r) g4[r] = make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int r = 0; r < kRowsPerWarp; ++r)
+                    g4[r] = g_mode == kGradPlain
+                                ? load_grad_plain(g_rows, gbi, gH, gW,
+                                                  (k * kRowsPerWarp + r) * kConsumerWarps + warp, col)
+                                : make_float4(0.f, 0.f, 0.f, 0.f);
             }
 
 #pragma unroll
@@ -814,7 +907,21 @@ extern "C" int fp8z_encode_grad_maps(const void* const* g_ptrs, const fp8z_param
         if (!g_ptrs[i] || pe.e < 1 || pe.rows < 1 || pe.cols < 1 || pe.e > 0x7FFFFFFFLL ||
             pe.rows > 0xFFFFFFFFLL || pe.cols > 0xFFFFFFFFLL)
             return FP8Z_EINVAL;
-        if (!host::aligned(g_ptrs[i], 16) || (pe.cols * 4) % 16 != 0) return FP8Z_EALIGN;
+        if ((pe.cols * 4) % 16 != 0) {
+            // no tensor map can step over these rows: the slot holds a record
+            // for plain loads instead
+            if (!host::aligned(g_ptrs[i], 4)) return FP8Z_EALIGN;
+            PlainGrad rec;
+            std::memset(&rec, 0, sizeof(rec));
+            rec.magic = kPlainGradMagic;
+            rec.ptr = static_cast<const float*>(g_ptrs[i]);
+            rec.e = pe.e;
+            rec.rows = pe.rows;
+            rec.cols = pe.cols;
+            std::memcpy(&maps[i], &rec, sizeof(rec));
+            continue;
+        }
+        if (!host::aligned(g_ptrs[i], 16)) return FP8Z_EALIGN;
         const cuuint64_t dims[3] = {cuuint64_t(pe.cols), cuuint64_t(pe.rows), cuuint64_t(pe.e)};
         const cuuint64_t strides[2] = {cuuint64_t(pe.cols * 4), cuuint64_t(pe.rows * pe.cols * 4)};
         const cuuint32_t boxd[3] = {kBlk, kStageRows, 1};

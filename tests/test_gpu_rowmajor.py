@@ -127,8 +127,50 @@ def test_rowmajor_bad_descriptor_reported(oracle):
     assert run_case(oracle, [(1, 256, 256)], dp=1, bad_desc=True) == fp8z.FP8Z_EINVAL
 
 
-def test_encode_grad_maps_rejects_unaligned_rows():
-    params, _, _, _ = fp8z.fp8z_plan_shards([(1, 128, 130)], 1, 0, with_blocks=False)
-    g = torch.zeros((1, 128, 130), device="cuda")
+# grads whose row pitch is not a multiple of 16 bytes (cols % 4 != 0) are read
+# with plain loads; mixed with tensor-map params in one launch
+UNALIGNED = [(1, 300, 1), (1, 256, 384), (2, 129, 7), (1, 200, 130), (1, 130, 1001), (1, 64, 64)]
+
+
+@pytest.mark.parametrize("transposed", [False, True])
+@pytest.mark.parametrize("dp,split", [(1, 0), (3, 0), (4, 1)])
+def test_rowmajor_step_unaligned_rows(oracle, transposed, dp, split):
+    run_case(oracle, UNALIGNED, dp=dp, split=split, transposed=transposed, seed=dp + 7)
+
+
+def test_rowmajor_step_unaligned_rows_pow2_post_decay(oracle):
+    run_case(oracle, [(3, 7, 1001), (1, 1000, 129)], dp=2, transposed=True, seed=3,
+             hp_kw=dict(step=20, scale_mode=1, decay_mode=1))
+
+
+def test_encode_grad_maps_alignment_rules():
+    # a tensor-map grad must start on 16 bytes; a plain-load grad on 4
+    params, _, _, _ = fp8z.fp8z_plan_shards([(1, 128, 132)], 1, 0, with_blocks=False)
+    g = torch.zeros(128 * 132 + 1, device="cuda")
     with pytest.raises(fp8z.Fp8zError):
-        fp8z.fp8z_encode_grad_maps([g], params)
+        fp8z.fp8z_encode_grad_maps([g[1:]], params)
+    params, _, _, _ = fp8z.fp8z_plan_shards([(1, 128, 130)], 1, 0, with_blocks=False)
+    fp8z.fp8z_encode_grad_maps([g[1:1 + 128 * 130]], params)
+
+
+@pytest.mark.parametrize("enc_cols,run_cols", [(130, 132), (132, 130)])
+def test_rowmajor_slot_of_another_shape_is_reported(enc_cols, run_cols):
+    """Slots encoded for one shape used with a param table of another: a record
+    where a tensor map belongs, or the reverse, gives grad 0 and FP8Z_EINVAL
+    (the kernel reads neither through a slot that does not match)."""
+    dev = torch.device("cuda")
+    p_enc, _, _, _ = fp8z.fp8z_plan_shards([(1, 256, enc_cols)], 1, 0, with_blocks=False)
+    g = torch.randn(256 * max(enc_cols, run_cols), device=dev)
+    maps = fp8z.fp8z_encode_grad_maps([g], p_enc)
+    params, shards, blocks, summ = fp8z.fp8z_plan_shards([(1, 256, run_cols)], 1, 0)
+    cap = int(summ["capacity_blocks"])
+    p, m, v = (torch.zeros(cap * BLK, device=dev) for _ in range(3))
+    w_row = torch.zeros(256 * run_cols, dtype=torch.uint8, device=dev)
+    inv = torch.zeros(cap, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    fp8z.fp8z_adamw_requant_step_rowmajor(p, m, v, maps, w_row, inv, 0, cap, fp8z.hparams(),
+                                          fp8z.table_to_device(blocks), fp8z.table_to_device(params), 1,
+                                          dev_status=st)
+    torch.cuda.synchronize()
+    assert st.item() == fp8z.FP8Z_EINVAL
+    assert int(m.count_nonzero()) == 0          # grad 0 and m 0: m stays 0
