@@ -402,6 +402,15 @@ def run_ours(args):
                                             shards, hp_kw, t, dev, ws)
     torch.cuda.nvtx.range_pop()
 
+    # ---- the other workloads, after this one's buffers are freed
+    configs = None
+    if not args.no_configs and w.name == "flat6e9":
+        del state, q, inv, wt, it, desc, pdev
+        torch.cuda.empty_cache()
+        torch.cuda.nvtx.range_push("configs")
+        configs = run_configs(args, dev, stream, peak)
+        torch.cuda.nvtx.range_pop()
+
     line = {
         "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 4),
@@ -425,6 +434,7 @@ def run_ours(args):
                      "kernel": "fp8z_step_kernel", "kernel_ms": round(avg_launch_s * 1e3, 4)},
         "aux_kernels": aux,
         "shard_timing": shard_timing,
+        "configs": configs,
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
         "e2e": e2e,
@@ -441,12 +451,10 @@ def run_ours(args):
 def time_aux_kernels(w, q, inv, params, dev, stream, peak, reps=5, g=None, fused=None):
     """Dequantize, the standalone column-major transpose, unfold/fold of the
     FP32 grad, the fused row-major step, unfold of the E4M3 codes, and the 1x128
-    row-wise quantize + scaling-aware transpose of a 65536x7168 activation, each
-    timed with CUDA events against its algorithmic bytes (dequant: 1 B read + 4 B
-    written per element + 4 B per block; transpose: 1 + 1 B per element + 8 B per
-    block; FP32 fold/unfold: 4 + 4 B per element; byte unfold: 1 + 1 B per
-    element; row-wise quantize: 4 + 1 B per element + 4 B per 128; row-wise
-    transpose: 1 + 1 B per element + 8 B per 128)."""
+    row-wise kernels (rowwise_study), each timed with CUDA events against its
+    algorithmic bytes (dequant: 1 B read + 4 B written per element + 4 B per
+    block; transpose: 1 + 1 B per element + 8 B per block; FP32 fold/unfold:
+    4 + 4 B per element; byte unfold: 1 + 1 B per element)."""
     import torch
     from blockwise_fp8_zero_gb300 import fp8z
     out = {}
@@ -513,86 +521,146 @@ def time_aux_kernels(w, q, inv, params, dev, stream, peak, reps=5, g=None, fused
         qb = torch.empty(E * H * W, dtype=torch.uint8, device=dev)
         timed(lambda: fp8z.fp8z_unfold(q, pe, qb, stream=stream), 2 * E * H * W, "fp8z_unfold_e4m3")
         del qb
-    # 1x128 row-wise quantize + scaling-aware transpose of an activation of
-    # 65536 tokens x 7168 (N(0,1), 0.1 % x60 outliers), power-of-two scales
     try:
-        T, Hd = 65536, 7168
-        gen = torch.Generator(device=dev)
-        gen.manual_seed(5)
-        xa = torch.randn(T, Hd, generator=gen, device=dev)
-        xa = torch.where(torch.rand(T, Hd, generator=gen, device=dev) < 1e-3, xa * 60, xa)
+        out.update(rowwise_study(dev, stream, peak))
+    except RuntimeError:
+        pass
+    return out
+
+
+def _activation(T, Hd, dev, seed=5):
+    """An activation of T tokens x Hd: N(0,1) with 0.1 % outliers x60."""
+    import torch
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(seed)
+    x = torch.randn(T, Hd, generator=gen, device=dev)
+    return torch.where(torch.rand(T, Hd, generator=gen, device=dev) < 1e-3, x * 60, x)
+
+
+def rowwise_study(dev, stream, peak, reps=5):
+    """1x128 row-wise quantization and the two ways to the column-wise layout
+    ("FP8-Flow-MoE" §3.1): the scaling-aware transpose, and the naive
+    dequantize -> transpose -> quantize, both run from the library's kernels
+    (the naive path: fp8z_dequant_rowwise with its transposed output, then
+    fp8z_quantize_rowwise; its dequantize and transpose share one pass, which
+    can only make it faster).  Timed at T x 7168 activations for several T
+    (power-of-two scales, the page's setting for its speed comparison), with
+    each kernel's algorithmic bytes: quantize 4 + 1 B per element + 4 B per
+    128; scaling-aware transpose 1 + 1 B per element + 8 B per 128; transposed
+    dequantize 1 + 4 B per element + 4 B per 128."""
+    import torch
+    from blockwise_fp8_zero_gb300 import fp8z
+    out = {}
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+
+    def timed(fn):
+        with torch.cuda.stream(stream):
+            fn()
+            ev[0].record(stream)
+            for _ in range(reps):
+                fn()
+            ev[1].record(stream)
+        torch.cuda.synchronize(dev)
+        return ev[0].elapsed_time(ev[1]) / reps
+
+    def entry(ms, nbytes, param):
+        return {"ms": round(ms, 4), "bytes": nbytes, "gbs": round(nbytes / ms / 1e6, 1),
+                "frac": round(nbytes / ms / 1e6 / peak, 4), "param": param}
+
+    Hd = 7168
+    sweep = {}
+    for T in (4096, 16384, 65536):
+        x = _activation(T, Hd, dev)
+        n = T * Hd
         qa = torch.empty(T, Hd, dtype=torch.uint8, device=dev)
         sa = torch.empty(T, Hd // 128, device=dev)
         qta = torch.empty(Hd, T, dtype=torch.uint8, device=dev)
         sta = torch.empty(Hd, T // 128, device=dev)
-    except RuntimeError:
-        return out
-    n = T * Hd
-
-    def timed_act(fn, nbytes, label):
-        timed(fn, nbytes, label)
-        out[label]["param"] = f"{T}x{Hd} activation"
-
-    timed_act(lambda: fp8z.fp8z_quantize_rowwise(xa, True, qa, sa, stream=stream), 5 * n + 4 * n // 128,
-              "fp8z_quantize_rowwise")
-    timed_act(lambda: fp8z.fp8z_transpose_rowwise(qa, sa, qta, sta, stream=stream), 2 * n + 8 * n // 128,
-              "fp8z_transpose_rowwise")
-    del qa, sa, qta, sta
-    try:
-        out["rowwise_double_quantization"] = rowwise_error_study(xa, stream)
-    except RuntimeError:
-        pass
-    del xa
+        xt = torch.empty(Hd, T, device=dev)
+        ms_q = timed(lambda: fp8z.fp8z_quantize_rowwise(x, True, qa, sa, stream=stream))
+        ms_sa = timed(lambda: fp8z.fp8z_transpose_rowwise(qa, sa, qta, sta, stream=stream))
+        ms_dt = timed(lambda: fp8z.fp8z_dequant_rowwise(qa, sa, xt, transpose=True, stream=stream))
+        ms_qt = timed(lambda: fp8z.fp8z_quantize_rowwise(xt, True, qta, sta, stream=stream))
+        param = f"{T}x{Hd} activation"
+        if T == 65536:
+            out["fp8z_quantize_rowwise"] = entry(ms_q, 5 * n + 4 * n // 128, param)
+            out["fp8z_transpose_rowwise"] = entry(ms_sa, 2 * n + 8 * n // 128, param)
+            out["fp8z_dequant_rowwise_transposed"] = entry(ms_dt, 5 * n + 4 * n // 128, param)
+        sweep[str(T)] = {"scaling_aware_ms": round(ms_sa, 4),
+                         "naive_dequant_transpose_requant_ms": round(ms_dt + ms_qt, 4),
+                         "naive_over_scaling_aware": round((ms_dt + ms_qt) / ms_sa, 3)}
+        del qa, sa, qta, sta, xt
+        if T != 65536:
+            del x
+    out["rowwise_transpose_speed"] = {
+        "by_tokens": sweep,
+        "note": "T x 7168 activations, power-of-two scales; naive = fp8z_dequant_rowwise (transposed "
+                "output) + fp8z_quantize_rowwise; the page reports 2-3x for its direct transpose "
+                "over dequantize-transpose-quantize (\"FP8-Flow-MoE\" §3.1, Figure 1)"}
+    out["naive_dequant_transpose_requant_ms"] = sweep["65536"]["naive_dequant_transpose_requant_ms"]
+    out["naive_over_scaling_aware"] = sweep["65536"]["naive_over_scaling_aware"]
+    out["rowwise_double_quantization"] = rowwise_error_study(x, stream)
+    del x
     return out
 
 
 def rowwise_error_study(x, stream):
-    """The double-quantization error ("FP8-Flow-MoE" §3.1) at the bench's
-    activation size: X quantized row-wise (1x128 tiles) by the library, then
-    brought to the column-wise layout three ways -- the library's
-    scaling-aware transpose; the naive path (dequantize, transpose, quantize
-    column-wise again, the quantize being the library's); and quantizing X^T
-    directly -- each compared with X^T.  Torch ops only decode codes and sum
-    errors here (measurement, not the path).  Reported per scale rule:
-    sum|v - X^T| / sum|X^T| for each layout, and the fraction of values that
-    differ from the row-layout values (re-rounded or underflowed)."""
+    """The double-quantization error of "FP8-Flow-MoE" §3.1 at the bench's
+    activation size, E = Q_col(D(Q_row(X))) - Q_col(X): X is quantized
+    row-wise (1x128 tiles), brought to the column-wise layout the naive way
+    (dequantize, transpose, quantize again), and compared with quantizing X^T
+    column-wise directly; the scaling-aware transpose of Q_row(X) is compared
+    with Q_col(X) the same way.  Every quantize, dequantize and transpose here
+    is the library's; torch ops only subtract and sum.  Per scale rule:
+    frac_codes_differ (codes of the two column-wise tensors), frac_values_differ
+    and rel_mean_abs_E = sum|E| / sum|X| on the dequantized values (the two
+    sides may carry different scales), for E_naive and for the scaling-aware
+    E_sa = SA(Q_row(X)) - Q_col(X)."""
     import torch
     from blockwise_fp8_zero_gb300 import fp8z
     T, Hd = x.shape
-
-    def decode(q, s):
-        return q.view(torch.float8_e4m3fn).float() * s.repeat_interleave(128, dim=1)
+    dev = x.device
 
     def quant(v, pow2):
-        q = torch.empty(v.shape, dtype=torch.uint8, device=v.device)
-        sc = torch.empty(v.shape[0], v.shape[1] // 128, device=v.device)
+        q = torch.empty(v.shape, dtype=torch.uint8, device=dev)
+        sc = torch.empty(v.shape[0], v.shape[1] // 128, device=dev)
         fp8z.fp8z_quantize_rowwise(v, pow2, q, sc, stream=stream)
         return q, sc
+
+    def dq(q, sc, transpose=False):
+        r, c = q.shape
+        o = torch.empty((c, r) if transpose else (r, c), device=dev)
+        fp8z.fp8z_dequant_rowwise(q, sc, o, transpose=transpose, stream=stream)
+        return o
 
     res = {}
     with torch.cuda.stream(stream):
         xt = x.t().contiguous()
-        denom = xt.abs().double().sum()
-        rel = lambda v: float((v.double() - xt.double()).abs().sum() / denom)
+        denom = float(xt.abs().double().sum())
         for name, pow2 in (("pow2_scales", True), ("amax448_scales", False)):
-            q, sc = quant(x, pow2)
-            v_row_t = decode(q, sc).t().contiguous()        # the row-layout values, transposed
-            qt = torch.empty(Hd, T, dtype=torch.uint8, device=x.device)
-            st = torch.empty(Hd, T // 128, device=x.device)
-            fp8z.fp8z_transpose_rowwise(q, sc, qt, st, stream=stream)
-            v_sa = decode(qt, st)
-            del q, sc, qt, st
-            v_naive = decode(*quant(v_row_t, pow2))
-            v_direct = decode(*quant(xt, pow2))
-            res[name] = {"err_scaling_aware": round(rel(v_sa), 6), "err_naive": round(rel(v_naive), 6),
-                         "err_direct": round(rel(v_direct), 6),
-                         "changed_scaling_aware": round(float((v_sa != v_row_t).double().mean()), 6),
-                         "changed_naive": round(float((v_naive != v_row_t).double().mean()), 6)}
-            del v_row_t, v_sa, v_naive, v_direct
+            q_row, s_row = quant(x, pow2)
+            q_dir, s_dir = quant(xt, pow2)                          # Q_col(X)
+            v_dir = dq(q_dir, s_dir)
+            q_nv, s_nv = quant(dq(q_row, s_row, transpose=True), pow2)   # Q_col(D(Q_row(X)))
+            q_sa = torch.empty(Hd, T, dtype=torch.uint8, device=dev)
+            s_sa = torch.empty(Hd, T // 128, device=dev)
+            fp8z.fp8z_transpose_rowwise(q_row, s_row, q_sa, s_sa, stream=stream)
+            row = {}
+            for tag, (q2, s2) in (("naive", (q_nv, s_nv)), ("scaling_aware", (q_sa, s_sa))):
+                e = dq(q2, s2) - v_dir
+                row[f"frac_codes_differ_{tag}"] = round(float((q2 != q_dir).double().mean()), 6)
+                row[f"frac_values_differ_{tag}"] = round(float((e != 0).double().mean()), 6)
+                row[f"rel_mean_abs_E_{tag}"] = round(float(e.abs().double().sum()) / denom, 7)
+                del e
+            # the row-wise values themselves against X (one quantization)
+            row["rel_err_row_layout"] = round(float((dq(q_row, s_row) - x).abs().double().sum()) / denom, 6)
+            res[name] = row
+            del q_row, s_row, q_dir, s_dir, v_dir, q_nv, s_nv, q_sa, s_sa
     torch.cuda.synchronize()
     res["param"] = f"{T}x{Hd} activation"
-    res["note"] = ("err_* = sum|v - X^T| / sum|X^T|; changed_* = fraction of values that differ "
-                   "from the row-layout values")
+    res["note"] = ("E = Q_col(D(Q_row(X))) - Q_col(X) on dequantized values; rel_mean_abs_E = "
+                   "sum|E| / sum|X|; *_scaling_aware: the same with the scaling-aware transpose in "
+                   "place of the naive path")
     return res
 
 
@@ -728,6 +796,93 @@ def run_e2e(args, w, state, q, inv, wt, it, desc, pdev, params, shards, hp_kw, t
             "note": "grads in, E4M3 weights + scales out per step; FP32 state resident"}
 
 
+CONFIG_RUNS = [("single_256x384", None), ("dense_h7168", None), ("moe64", None),
+               ("mixed500", 1), ("mixed500", 0)]
+
+
+def run_configs(args, dev, stream, peak, reps=10):
+    """The step on the other workloads, one after another in this process (each
+    freed before the next): per-shard launches (the whole model's step as D
+    launches, one per shard), all shards as one launch (shard padding masked by
+    the descriptors), and the rank-0 shard alone, the per-rank optimizer step a
+    DP rank would run.  Bytes: 29 B per element of every block a launch
+    processes (16 read, 13 written) + 24 B per block (descriptor, scale)."""
+    import torch
+    from blockwise_fp8_zero_gb300 import fp8z, workloads
+    res = {}
+    for name, split in CONFIG_RUNS:
+        w = workloads.get(name, split)
+        key = name if split is None else f"{name}_{'paramwise' if split == 1 else 'blockwise'}"
+        params, shards, blocks, summ = fp8z.fp8z_plan_shards(w.shapes, w.dp, w.split)
+        cap = int(summ["capacity_blocks"])
+        free, _ = torch.cuda.mem_get_info(dev)
+        if cap * BLK * 17 + (4 << 30) > free:
+            res[key] = {"skipped": f"needs {cap * BLK * 17 / 1e9:.0f} GB, {free / 1e9:.0f} GB free"}
+            continue
+        state = workloads.make_state(w, blocks, dev, seed=0)
+        q = torch.empty(cap * BLK, dtype=torch.uint8, device=dev)
+        inv = torch.empty(cap, dtype=torch.float32, device=dev)
+        desc = fp8z.table_to_device(blocks, dev)
+        status = torch.zeros(1, dtype=torch.int32, device=dev)
+        hp = fp8z.hparams(**w.hp)
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+
+        def timed(ranges):
+            def go():
+                for b0, nb in ranges:
+                    fp8z.fp8z_adamw_requant_step(state["p"], state["g"], state["m"], state["v"], q, inv, b0,
+                                                 nb, hp, desc=desc, dev_status=status, stream=stream)
+            with torch.cuda.stream(stream):
+                for _ in range(3):
+                    go()
+                ev[0].record(stream)
+                for _ in range(reps):
+                    go()
+                ev[1].record(stream)
+            torch.cuda.synchronize(dev)
+            return ev[0].elapsed_time(ev[1]) / reps
+
+        shard_ranges = [(int(sh["blk_begin"]), int(sh["blk_count_real"])) for sh in shards]
+        real = int(summ["real_elems"])
+        nreal = int(summ["total_blocks"])
+        per_block = BLK * 29 + 24
+        ms = timed(shard_ranges)
+        entry = {"dp_shards": w.dp, "split": "param-wise" if w.split == 1 else "block-wise",
+                 "params": len(w.shapes), "elements": real, "blocks": nreal, "capacity_blocks": cap,
+                 "padding_bytes_fp32_state": int(summ["fold_pad_elems"] + summ["shard_pad_elems"]) * 16,
+                 "fold_pad_elems": int(summ["fold_pad_elems"]),
+                 "shard_pad_elems": int(summ["shard_pad_elems"]),
+                 "launches": len(shards), "ms": round(ms, 4),
+                 "gelem_s": round(real / (ms / 1e3) / 1e9, 4),
+                 "gbs": round(nreal * per_block / ms / 1e6, 1),
+                 "frac": round(nreal * per_block / ms / 1e6 / peak, 4)}
+        if len(shards) > 1:
+            one_ms = timed([(0, cap)])
+            a0, n0 = shard_ranges[0]
+            r0_ms = timed([(a0, n0)])
+            r0_real = int(np.sum(blocks["valid_rows"][a0:a0 + n0].astype(np.int64)
+                                 * blocks["valid_cols"][a0:a0 + n0].astype(np.int64)))
+            entry["shard_timing"] = {
+                "per_shard_launches_ms": round(ms, 4),
+                "all_shards_one_launch_ms": round(one_ms, 4),
+                "all_shards_one_launch_gelem_s": round(real / (one_ms / 1e3) / 1e9, 4),
+                "all_shards_one_launch_frac": round(cap * per_block / one_ms / 1e6 / peak, 4),
+                "rank0_shard_ms": round(r0_ms, 4), "rank0_blocks": n0,
+                "rank0_gelem_s": round(r0_real / (r0_ms / 1e3) / 1e9, 4),
+                "rank0_gbs": round(n0 * per_block / r0_ms / 1e6, 1),
+                "rank0_frac": round(n0 * per_block / r0_ms / 1e6 / peak, 4)}
+        else:
+            entry["us"] = round(ms * 1e3, 2)
+        if status.item() != 0:
+            raise RuntimeError(f"{key}: {fp8z.fp8z_status_string(status.item())}")
+        res[key] = entry
+        del state, q, inv, desc, status
+        torch.cuda.empty_cache()
+    res["note"] = ("no column-major copy (only the flat 6e9 workload carries one); the same kernel, "
+                   "hyper-parameters of each workload; frac of the measured copy bandwidth")
+    return res
+
+
 def cpu_baseline(w, hp_kw, args, threads=None):
     threads = threads or (os.cpu_count() or 1)
     nblocks = args.cpu_blocks
@@ -789,6 +944,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-aux", action="store_true", help="skip the dequant/transpose timings")
+    ap.add_argument("--no-configs", action="store_true", help="skip the other workloads' step timings")
     ap.add_argument("--max-elems", type=int, default=0,
                     help="run a smaller workload of the same kind (profiling cases)")
     args = ap.parse_args()

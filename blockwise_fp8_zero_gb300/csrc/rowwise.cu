@@ -338,10 +338,114 @@ __global__ void __launch_bounds__(256, 3) transpose_rowwise_kernel(const uint8_t
     }
 }
 
+// ------------------------------------------------------ row-wise dequantize
+// "FP8-Flow-MoE" §3.1: D(Q(x)) = Q(x) * s, here decode(q[r][c]) * s[r][c/128]
+// in FP32 (the decode is exact, the product rounds once).  The first step of
+// the naive way to the column-wise layout (dequantize, transpose, quantize
+// again), kept so that path can be run and timed from the library's own
+// kernels.  HBM-bound: 1 B read + 4 B written per element.
+//
+// Row-major output: each thread turns 16 codes (one 16-byte load, which never
+// crosses a 128-column tile) into four 16-byte streaming stores.
+__global__ void __launch_bounds__(256) dequant_rowwise_kernel(const uint8_t* __restrict__ q,
+                                                              const float* __restrict__ s, int64_t nchunks,
+                                                              int64_t C, float* __restrict__ x) {
+    const int64_t per_row = C / 16, nt = C / kTile;
+    const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+    for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < nchunks; i += stride) {
+        const uint4 w = ld_stream_l2_256(reinterpret_cast<const uint4*>(q) + i);
+        const int64_t r = i / per_row, c = (i % per_row) * 16;
+        const float sc = __ldg(s + r * nt + c / kTile);
+        float4* dst = reinterpret_cast<float4*>(x + r * C + c);
+        const uint32_t words[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float2 lo = e4m3x2_to_float2(words[k]), hi = e4m3x2_to_float2(words[k] >> 16);
+            __stcs(dst + k, make_float4(__fmul_rn(lo.x, sc), __fmul_rn(lo.y, sc), __fmul_rn(hi.x, sc),
+                                        __fmul_rn(hi.y, sc)));
+        }
+    }
+}
+
+// Transposed output, out[c][r] = decode(q[r][c]) * s[r][c/128]: dequantize and
+// transpose of the naive path in one pass.  One CTA per 128x128 tile: the
+// tile's codes are staged in a swizzled shared tile, then lane l of every warp
+// takes input rows 4l..4l+3 (with their four row scales) and, per group of
+// four input columns, byte-transposes four words and writes four output rows,
+// a warp storing 512 contiguous bytes of one output row.  Consecutive CTAs
+// take consecutive row tiles of one column tile, so their output rows continue
+// each other in memory.
+__global__ void __launch_bounds__(256) dequant_rowwise_t_kernel(const uint8_t* __restrict__ q,
+                                                                const float* __restrict__ s, int64_t R,
+                                                                int64_t C, float* __restrict__ xt) {
+    __shared__ uint32_t tile[kTile * 32];
+    const int64_t ntr = R / kTile, ntc = C / kTile;
+    const int64_t i = blockIdx.x % ntr, j = blockIdx.x / ntr;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const uint4* src = reinterpret_cast<const uint4*>(q + (i * kTile) * C + j * kTile);
+#pragma unroll
+    for (int it = 0; it < 4; ++it) {
+        const int idx = it * 256 + tid;                  // 16-byte chunk of the tile
+        const int r = idx >> 3, w0 = (idx & 7) * 4, sw = tile_swz(r);
+        const uint4 w = ld_stream_l2_256(src + r * (C / 16) + (idx & 7));
+        tile[r * 32 + ((w0 + 0) ^ sw)] = w.x;
+        tile[r * 32 + ((w0 + 1) ^ sw)] = w.y;
+        tile[r * 32 + ((w0 + 2) ^ sw)] = w.z;
+        tile[r * 32 + ((w0 + 3) ^ sw)] = w.w;
+    }
+    const int r0 = lane * 4;
+    float sc[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) sc[k] = __ldg(s + (i * kTile + r0 + k) * ntc + j);
+    __syncthreads();
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+        const int cg = warp + 8 * h;                     // input columns 4cg..4cg+3
+        uint32_t w4[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) w4[k] = tile[(r0 + k) * 32 + (cg ^ tile_swz(r0 + k))];
+        uint32_t o[4];
+        transpose4x4(w4[0], w4[1], w4[2], w4[3], o[0], o[1], o[2], o[3]);
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {                 // output row j*128 + 4cg + cc
+            const float2 lo = e4m3x2_to_float2(o[cc]), hi = e4m3x2_to_float2(o[cc] >> 16);
+            float4* dst = reinterpret_cast<float4*>(xt + (j * kTile + 4 * cg + cc) * R + i * kTile + r0);
+            __stcs(dst, make_float4(__fmul_rn(lo.x, sc[0]), __fmul_rn(lo.y, sc[1]), __fmul_rn(hi.x, sc[2]),
+                                    __fmul_rn(hi.y, sc[3])));
+        }
+    }
+}
+
 }  // namespace
 }  // namespace fp8z
 
 using namespace fp8z;
+
+extern "C" int fp8z_dequant_rowwise(const uint8_t* q, const float* s, int64_t rows, int64_t cols,
+                                    int32_t transpose, float* out, void* stream) {
+    const fp8z::host::NvtxRange nvtx_range("fp8z_dequant_rowwise");
+    if (!q || !s || !out || rows < 0 || cols < 0 || cols % kTile || (transpose != 0 && transpose != 1))
+        return FP8Z_EINVAL;
+    if (transpose && rows % kTile) return FP8Z_EINVAL;
+    if (rows > (INT64_MAX / 4) / (cols > 0 ? cols : 1)) return FP8Z_EINVAL;
+    if (!host::aligned(q, 16) || !host::aligned(out, 16) || !host::aligned(s, 4)) return FP8Z_EALIGN;
+    const int64_t n = rows * cols;
+    if (n == 0) return FP8Z_OK;
+    int sms = 0;
+    const int rc = host::device_sms(&sms);
+    if (rc != FP8Z_OK) return rc;
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (transpose) {
+        const int64_t ntiles = (rows / kTile) * (cols / kTile);
+        if (ntiles > 0x7FFFFFFFLL) return FP8Z_EINVAL;
+        dequant_rowwise_t_kernel<<<unsigned(ntiles), 256, 0, st>>>(q, s, rows, cols, out);
+    } else {
+        const int64_t nchunks = n / 16;
+        const int64_t want = (nchunks + 255) / 256, cap = int64_t(sms) * 8;
+        dequant_rowwise_kernel<<<unsigned(want < cap ? want : cap), 256, 0, st>>>(q, s, nchunks, cols, out);
+    }
+    return cudaGetLastError() == cudaSuccess ? FP8Z_OK : FP8Z_ECUDA;
+}
 
 extern "C" int fp8z_quantize_rowwise(const float* x, int64_t rows, int64_t cols, int32_t pow2,
                                      uint8_t* q, float* s, void* stream) {

@@ -47,7 +47,7 @@ EXPORTED = ("fp8z_plan_shards", "fp8z_adamw_requant_step", "fp8z_adamw_requant_s
             "fp8z_adamw_requant_step_mx", "fp8z_adamw_requant_step_rowmajor_static",
             "fp8z_encode_grad_maps", "fp8z_dequant",
             "fp8z_transpose_fp8", "fp8z_fold", "fp8z_unfold", "fp8z_quantize_rowwise",
-            "fp8z_transpose_rowwise", "fp8z_e4m3_encode_bits",
+            "fp8z_transpose_rowwise", "fp8z_dequant_rowwise", "fp8z_e4m3_encode_bits",
             "fp8z_watchdog_selftest", "fp8z_set_wait_limit_ns", "fp8z_get_wait_limit_ns",
             "fp8z_status_string")
 
@@ -108,6 +108,7 @@ def lib():
         L.fp8z_unfold.argtypes = [P, i32, P, P, P, P]
         L.fp8z_quantize_rowwise.argtypes = [P, i64, i64, i32, P, P, P]
         L.fp8z_transpose_rowwise.argtypes = [P, P, i64, i64, P, P, P]
+        L.fp8z_dequant_rowwise.argtypes = [P, P, i64, i64, i32, P, P]
         L.fp8z_e4m3_encode_bits.argtypes = [ctypes.c_uint32, i64, P, P]
         L.fp8z_watchdog_selftest.argtypes = [P, i64, P]
         L.fp8z_set_wait_limit_ns.argtypes = [i64]
@@ -431,6 +432,19 @@ def fp8z_transpose_rowwise(q, s, q_t, s_t, stream=None):
                                       _dptr(q_t, torch.uint8, "q_t"), _dptr(s_t, torch.float32, "s_t"),
                                       _stream_handle(stream))
     _check("fp8z_transpose_rowwise", rc)
+
+
+def fp8z_dequant_rowwise(q, s, out, transpose=False, stream=None):
+    """Row-wise codes q [rows, cols] and scales s [rows, cols/128] -> float32 out
+    [rows, cols], or [cols, rows] when transpose is set."""
+    import torch
+    rows, cols = q.shape
+    if out.numel() < rows * cols or s.numel() < rows * (cols // BLOCK):
+        raise ValueError("buffers too small")
+    rc = lib().fp8z_dequant_rowwise(_dptr(q, torch.uint8, "q"), _dptr(s, torch.float32, "s"), rows, cols,
+                                    int(bool(transpose)), _dptr(out, torch.float32, "out"),
+                                    _stream_handle(stream))
+    _check("fp8z_dequant_rowwise", rc)
 
 
 def fp8z_e4m3_encode_bits(first_bits, n, out, stream=None):

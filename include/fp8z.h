@@ -202,8 +202,11 @@ FP8Z_API int fp8z_adamw_requant_step(float *p, const float *g, float *m, float *
  * into the param's row-major [e, rows, cols] bytes.  p, m, v stay folded (the
  * optimizer's own state), inv_scale is per folded block (already the
  * row-major [e, hb, wb] grid of each param).
- * g_maps: device array of nparams tensor maps (128 bytes each, 64-byte
- *   aligned) written by fp8z_encode_grad_maps and copied to the device.
+ * g_maps: device array of the nparams 128-byte slots (64-byte aligned)
+ *   written by fp8z_encode_grad_maps and copied to the device.  Grads whose
+ *   cols is not a multiple of 4 are read with plain loads instead of the TMA
+ *   engine (slower, same results); a slot that does not match its param entry
+ *   gives that param's blocks grad 0 and FP8Z_EINVAL in *dev_status.
  * w_row / w_row_bytes: device buffer of every param's row-major E4M3 bytes,
  *   param i at params[i].t_offset (the same offsets as the column-major copy).
  * desc and params (device) are required.  Other arguments, per-element math,
@@ -283,12 +286,16 @@ FP8Z_API int fp8z_adamw_requant_step_mx(float *p, const float *g, float *m, floa
                                         void *stream);
 
 /*
- * fp8z_encode_grad_maps -- host only: the tensor maps the row-major step reads
- * the grads through.  g_ptrs[i] (host array of device pointers) is param i's
- * row-major FP32 grad [e, rows, cols]; params[i] its planner entry (host).
- * Writes nparams maps of 128 bytes to maps_out (host, 64-byte aligned); the
- * caller copies them to device memory.  Each grad must be 16-byte aligned with
- * cols a multiple of 4 (FP8Z_EALIGN otherwise).  No device work.
+ * fp8z_encode_grad_maps -- host only: the 128-byte slots the row-major step
+ * reads the grads through.  g_ptrs[i] (host array of device pointers) is
+ * param i's row-major FP32 grad [e, rows, cols]; params[i] its planner entry
+ * (host).  Writes nparams slots of 128 bytes to maps_out (host, 64-byte
+ * aligned); the caller copies them to device memory.  When cols is a multiple
+ * of 4 the slot is a TMA tensor map and the grad must be 16-byte aligned;
+ * otherwise (a row pitch the TMA engine cannot step over) the slot records
+ * the grad's address and shape, the kernel reads that grad with plain loads,
+ * and the grad must be 4-byte aligned.  FP8Z_EALIGN for a misaligned grad.
+ * The slots must be used with the same param table.  No device work.
  */
 FP8Z_API int fp8z_encode_grad_maps(const void *const *g_ptrs, const fp8z_param_entry *params,
                                    int32_t nparams, void *maps_out);
@@ -376,6 +383,21 @@ FP8Z_API int fp8z_quantize_rowwise(const float *x, int64_t rows, int64_t cols, i
  */
 FP8Z_API int fp8z_transpose_rowwise(const uint8_t *q, const float *s, int64_t rows, int64_t cols,
                                     uint8_t *q_t, float *s_t, void *stream);
+
+/*
+ * fp8z_dequant_rowwise -- row-wise dequantize ("FP8-Flow-MoE" §3.1,
+ * D(Q(x)) = Q(x) * s): x[r][c] = E4M3_value(q[r][c]) * s[r][c/128] (float
+ * product).  With transpose = 1 the result is written transposed,
+ * out[c][r], which is the dequantize-then-transpose half of the naive way to
+ * the column-wise layout that the scaling-aware transpose avoids (the other
+ * half is fp8z_quantize_rowwise of out).  q: device u8 [rows, cols];
+ * s: device f32 [rows, cols/128]; out: device f32 [rows, cols], or
+ * [cols, rows] when transposed.  cols a multiple of 128 (rows too when
+ * transposed); q and out 16-byte aligned.
+ * Returns FP8Z_OK / EINVAL / EALIGN / EUNSUPPORTED / ECUDA.
+ */
+FP8Z_API int fp8z_dequant_rowwise(const uint8_t *q, const float *s, int64_t rows, int64_t cols,
+                                  int32_t transpose, float *out, void *stream);
 
 /*
  * fp8z_e4m3_encode_bits -- out[i] = E4M3 code (round to nearest even,

@@ -168,6 +168,11 @@ def test_rowwise_and_mx_argument_errors(L):
     assert L.fp8z_transpose_rowwise(A16, A16, 100, 128, A16, A16, None) == fp8z.FP8Z_EINVAL
     assert L.fp8z_transpose_rowwise(A16, A16, 128, 130, A16, A16, None) == fp8z.FP8Z_EINVAL
     assert L.fp8z_transpose_rowwise(A4, A16, 128, 128, A16, A16, None) == fp8z.FP8Z_EALIGN
+    assert L.fp8z_dequant_rowwise(A16, A16, 0, 128, 1, A16, None) == fp8z.FP8Z_OK
+    assert L.fp8z_dequant_rowwise(A16, A16, 4, 100, 0, A16, None) == fp8z.FP8Z_EINVAL
+    assert L.fp8z_dequant_rowwise(A16, A16, 100, 128, 1, A16, None) == fp8z.FP8Z_EINVAL   # rows % 128
+    assert L.fp8z_dequant_rowwise(A16, A16, 4, 128, 2, A16, None) == fp8z.FP8Z_EINVAL
+    assert L.fp8z_dequant_rowwise(A16, A16, 4, 128, 0, A4, None) == fp8z.FP8Z_EALIGN
     # MXFP8 step: same state checks as the block-scaled step, its own scale output
     hp = fp8z.hparams()
     mx = lambda **k: L.fp8z_adamw_requant_step_mx(

@@ -105,3 +105,53 @@ def test_rowwise_extreme_magnitudes(oracle, pow2):
     qto, sto = oracle.transpose_rowwise(qo, so)
     assert np.array_equal(st.cpu().numpy().view(np.uint32), sto.view(np.uint32))
     assert np.array_equal(qt.cpu().numpy(), qto)
+
+
+def _same_floats(a, b):
+    """Bitwise equal, NaN equal to NaN (the E4M3 NaN codes decode to NaN)."""
+    same = (a.view(np.uint32) == b.view(np.uint32)) | (np.isnan(a) & np.isnan(b))
+    assert np.all(same), f"{int((~same).sum())} differ"
+
+
+@pytest.mark.parametrize("shape", [(128, 128), (256, 384), (1000, 1280), (4096, 7168)])
+def test_dequant_rowwise(oracle, shape):
+    """Every code (NaN codes included) under power-of-two, amax/448-like,
+    subnormal-producing and near-FLT_MAX scales, row-major and transposed,
+    against the oracle's dequantize."""
+    R, C = shape
+    rng = np.random.default_rng(R + C)
+    q = rng.integers(0, 256, (R, C), dtype=np.uint8)
+    q[0, :256 if C >= 256 else C] = np.arange(min(C, 256), dtype=np.uint8)
+    s = (10.0 ** rng.uniform(-30, 30, (R, C // 128))).astype(np.float32)
+    s[::3] = np.exp2(rng.integers(-126, 120, s[::3].shape)).astype(np.float32)
+    s[1, 0] = 1e-40                                  # subnormal products
+    s[2, 0] = 3e38                                   # products overflow to infinity
+    want = oracle.dequant_rowwise(q, s)
+    qd, sd = torch.from_numpy(q).cuda(), torch.from_numpy(s).cuda()
+    out = torch.empty(R, C, device="cuda")
+    fp8z.fp8z_dequant_rowwise(qd, sd, out)
+    torch.cuda.synchronize()
+    _same_floats(out.cpu().numpy(), want)
+    if R % 128 == 0:
+        out_t = torch.empty(C, R, device="cuda")
+        fp8z.fp8z_dequant_rowwise(qd, sd, out_t, transpose=True)
+        torch.cuda.synchronize()
+        _same_floats(out_t.cpu().numpy(), np.ascontiguousarray(want.T))
+
+
+def test_naive_path_from_library_kernels(oracle):
+    """The naive way to the column-wise layout, dequantize-transpose then
+    quantize again, run from the library's kernels, equals the oracle's
+    quantize of the oracle's dequantized transpose."""
+    x = _act(512, 768, seed=4)
+    for pow2 in (True, False):
+        qo, so = oracle.quantize_rowwise(x.numpy(), pow2=pow2)
+        xt = torch.empty(768, 512, device="cuda")
+        fp8z.fp8z_dequant_rowwise(torch.from_numpy(qo).cuda(), torch.from_numpy(so).cuda(), xt, transpose=True)
+        qn = torch.empty(768, 512, dtype=torch.uint8, device="cuda")
+        sn = torch.empty(768, 4, device="cuda")
+        fp8z.fp8z_quantize_rowwise(xt, pow2, qn, sn)
+        torch.cuda.synchronize()
+        qw, sw = oracle.quantize_rowwise(np.ascontiguousarray(oracle.dequant_rowwise(qo, so).T), pow2=pow2)
+        assert np.array_equal(qn.cpu().numpy(), qw)
+        assert np.array_equal(sn.cpu().numpy().view(np.uint32), sw.view(np.uint32))
