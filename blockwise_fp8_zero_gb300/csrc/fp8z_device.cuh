@@ -54,6 +54,29 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return done != 0;
 }
 
+// The same test without suspending the thread at all: true once the phase
+// with the given parity has completed, false at once otherwise.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred P;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 P, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, P;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+// Below this limit a bounded wait polls with mbar_test_wait and measures the
+// wait in SM clock cycles (two per nanosecond: about the limit at the 2.07
+// GHz top clock, longer at lower clocks) instead of suspending in try_wait
+// and reading the global timer: a copy that lands within the hardware's own
+// suspend window, or within one tick of the global timer, would otherwise
+// never let a short limit be checked.  Limits this short are set only to
+// exercise the abort paths (fp8z_set_wait_limit_ns).
+constexpr int64_t kPolledWaitBelowNs = 1000000;
+
 // Shared state for the bounded waits of one CTA.
 struct Watchdog {
     volatile int* abort_flag;   // shared: set once any wait of the CTA gave up
@@ -70,6 +93,18 @@ __device__ __forceinline__ void report_status(int32_t* dev_status, int32_t code)
 // the limit is reached, or when another thread of the CTA has already
 // aborted.  Never spins without a limit.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, const Watchdog& wd) {
+    if (wd.timeout_ns < kPolledWaitBelowNs) {
+        const long long c0 = clock64();
+        while (true) {
+            if (mbar_test_wait(bar, parity)) return true;
+            if (*wd.abort_flag) return false;
+            if (clock64() - c0 > 2 * wd.timeout_ns) {
+                *wd.abort_flag = 1;
+                report_status(wd.dev_status, FP8Z_ETIMEOUT);
+                return false;
+            }
+        }
+    }
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     while (true) {
