@@ -101,7 +101,8 @@ constexpr size_t kCtxOffset = kRingBytes + kTileBytes + kAmaxBytes;
 constexpr size_t kCtxBytes = 2 * 96;                     // two BlockCtx slots
 constexpr size_t kBarOffset = kCtxOffset + kCtxBytes;
 constexpr int kNumBars = 2 * kRing + 2;
-constexpr size_t kSmemBytes = kBarOffset + kNumBars * 8 + 16;
+constexpr size_t kToutOffset = (kBarOffset + kNumBars * 8 + 16 + 127) / 128 * 128;
+constexpr size_t kSmemBytes = kToutOffset + kTileBytes;   // + the transposed output tile
 
 struct StepArgs {
     float* p;
@@ -305,6 +306,13 @@ __device__ __forceinline__ void store_word(uint8_t* dst, uint32_t x) {
     *reinterpret_cast<uint32_t*>(dst) = x;
 }
 
+// 16-byte global store carrying an L2 eviction policy.
+__device__ __forceinline__ void store_v4_hint(void* dst, uint4 x, uint64_t pol) {
+    asm volatile("st.global.L2::cache_hint.v4.b32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(dst), "r"(x.x), "r"(x.y),
+                 "r"(x.z), "r"(x.w), "l"(pol)
+                 : "memory");
+}
+
 // Which blocks a CTA owns: blocks are dealt round-robin, so at any moment the
 // CTAs stream neighbouring 64 KB blocks (DRAM page locality).  The grid never
 // exceeds nblk, so every CTA owns at least one block.
@@ -377,13 +385,35 @@ __device__ __forceinline__ float4 load_grad_plain(const float* g_rows, const Blo
 // of the ZeRO design page: the FP8 params are unfolded back to their 2-D/3-D
 // shape; here the unfold happens on the way out).  Row r of the block is 128
 // contiguous bytes of row brow*128 + r of the param; like the column-major
-// copy's, these scattered rows are stored with the L2 evict-last policy.
+// copy's, these scattered rows are stored with the L2 evict-last policy.  A
+// whole block whose rows start on 16 bytes is staged in the warp's own eight
+// rows of the linear output tile (the column-major copy has read them out at
+// the start of this block and refills them only at the next one), so that
+// each lane writes 16 bytes and a warp store covers four rows.
 __device__ __forceinline__ void store_rowmajor(const StepArgs& A, const BlockInfo& bi, const ParamInfo& pi,
-                                               const uint32_t (&words)[kKeep], int warp, int col) {
+                                               const uint32_t (&words)[kKeep], uint8_t* tout, int warp,
+                                               int lane, int col) {
     const int64_t H = pi.H, W = pi.W;
-    const int64_t base = pi.t_off + bi.e * H * W + int64_t(bi.brow) * kBlk * W + int64_t(bi.bcol) * kBlk;
-    const bool aligned = ((pi.t_off + bi.e * H * W) | W) % 4 == 0;
+    const int64_t pbase = pi.t_off + bi.e * H * W;
+    const int64_t base = pbase + int64_t(bi.brow) * kBlk * W + int64_t(bi.bcol) * kBlk;
     const uint64_t keep_in_l2 = l2_evict_last_policy();
+    if (bi.vr == kBlk && bi.vc == kBlk && ((pbase | W) & 15) == 0) {
+        // block row k * 16 + warp goes to tout row 4 * warp + k (k < 4) or
+        // 64 + 4 * warp + k - 4: the rows column_major_out gives this warp
+#pragma unroll
+        for (int k = 0; k < kKeep; ++k)
+            *reinterpret_cast<uint32_t*>(tout + ((k >> 2) * 64 + 4 * warp + (k & 3)) * 128 + col) = words[k];
+        __syncwarp();
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int k = 4 * h + (lane >> 3), ch = lane & 7;
+            const uint4 x = *reinterpret_cast<const uint4*>(tout + (h * 64 + 4 * warp + (lane >> 3)) * 128 + ch * 16);
+            store_v4_hint(A.w_row + base + int64_t(k * kConsumerWarps + warp) * W + ch * 16, x, keep_in_l2);
+        }
+        __syncwarp();
+        return;
+    }
+    const bool aligned = ((pi.t_off + bi.e * H * W) | W) % 4 == 0;
 #pragma unroll
     for (int k = 0; k < kKeep; ++k) {
         const int row = k * kConsumerWarps + warp;
@@ -398,15 +428,20 @@ __device__ __forceinline__ void store_rowmajor(const StepArgs& A, const BlockInf
 }
 
 // Column-major copy of one block: the quantized words go through a swizzled
-// shared tile; each warp then writes four output rows per pass, 128
-// contiguous bytes per warp store.  The stores carry an L2 evict-last policy:
-// a block adds 128 bytes to each of 128 output rows, and lines kept longer in
-// L2 meet their row neighbours from other blocks before they are written back
+// shared tile; each warp then takes four output rows (input columns) per pass
+// from 4x4 byte transposes.  The stores carry an L2 evict-last policy: a block
+// adds 128 bytes to each of 128 output rows, and lines kept longer in L2 meet
+// their row neighbours from other blocks before they are written back
 // (28.24 -> 27.93 ms per step on GB300 at 117 x 7168^2; 1.0 of the lines beat
-// 0.5 and 0.25).  column_major_in stages the block (false
-// when the descriptor does not match the param table: nothing is staged);
-// column_major_out waits until every warp has staged its rows and writes the
-// block out (false when that wait gave up).
+// 0.5 and 0.25).  A whole block whose output rows start on 16 bytes goes
+// through a second, linear shared tile (the warp's own output rows, 128 bytes
+// each) so that every lane writes 16 bytes and a warp store covers four output
+// rows: 28.21 -> 28.06 ms against 4-byte stores straight from the transposes
+// (a 128-byte bulk copy per output row, or one tensor-map store of the tile,
+// measured no faster, or 10 % slower).  column_major_in stages the block
+// (false when the descriptor does not match the param table: nothing is
+// staged); column_major_out waits until every warp has staged its rows and
+// writes the block out (false when that wait gave up).
 __device__ __forceinline__ bool column_major_in(const StepArgs& A, const BlockInfo& bi, const ParamInfo& pi,
                                                 const uint32_t (&words)[kKeep], float inv, uint32_t* tile,
                                                 uint32_t tile_bar, int tid, int warp, int lane) {
@@ -426,7 +461,7 @@ __device__ __forceinline__ bool column_major_in(const StepArgs& A, const BlockIn
 }
 
 __device__ __forceinline__ bool column_major_out(const StepArgs& A, const BlockInfo& bi, const ParamInfo& pi,
-                                                 const uint32_t* tile, uint32_t tile_bar,
+                                                 const uint32_t* tile, uint8_t* tout, uint32_t tile_bar,
                                                  uint32_t& tile_phase, const Watchdog& wd, int warp,
                                                  int lane) {
     if (!mbar_wait_bounded(tile_bar, tile_phase, wd)) return false;
@@ -434,9 +469,33 @@ __device__ __forceinline__ bool column_major_out(const StepArgs& A, const BlockI
     const uint64_t keep_in_l2 = l2_evict_last_policy();
     const int64_t H = pi.H;
     const int64_t t_base = pi.t_off + bi.e * H * pi.W;
-    const bool aligned = ((t_base | H) & 3) == 0;
     const int r0 = lane * 4;                           // input rows r0..r0+3
     uint8_t* out_blk = A.w_fp8_t + t_base + bi.brow * int64_t(kBlk);
+    if (bi.vr == kBlk && bi.vc == kBlk && ((t_base | H) & 15) == 0) {
+        // a warp writes and reads back only its own eight rows of tout, so
+        // the warp barrier orders both and no other warp touches them
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int cg = warp + h * kConsumerWarps;  // input cols 4cg..4cg+3
+            uint32_t w4[4];
+#pragma unroll
+            for (int ii = 0; ii < 4; ++ii) w4[ii] = tile[(r0 + ii) * 32 + (cg ^ tile_swz(r0 + ii))];
+            uint32_t o[4];
+            transpose4x4(w4[0], w4[1], w4[2], w4[3], o[0], o[1], o[2], o[3]);
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) *reinterpret_cast<uint32_t*>(tout + (4 * cg + cc) * 128 + r0) = o[cc];
+        }
+        __syncwarp();
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int c = 4 * (warp + h * kConsumerWarps) + (lane >> 3), ch = lane & 7;
+            const uint4 x = *reinterpret_cast<const uint4*>(tout + c * 128 + ch * 16);
+            store_v4_hint(out_blk + (bi.bcol * int64_t(kBlk) + c) * H + ch * 16, x, keep_in_l2);
+        }
+        __syncwarp();
+        return true;
+    }
+    const bool aligned = ((t_base | H) & 3) == 0;
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
         const int cg = warp + h * kConsumerWarps;      // input cols 4cg..4cg+3
@@ -465,6 +524,7 @@ __global__ void __launch_bounds__(kThreads, 1) fp8z_step_kernel(const StepArgs A
     extern __shared__ __align__(1024) unsigned char smem[];
     float* ring = reinterpret_cast<float*>(smem);
     uint32_t* tile = reinterpret_cast<uint32_t*>(smem + kRingBytes);
+    uint8_t* tout = smem + kToutOffset;
     float* amax_x = reinterpret_cast<float*>(smem + kRingBytes + kTileBytes);
     BlockCtx* ctx = reinterpret_cast<BlockCtx*>(smem + kCtxOffset);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kBarOffset);
@@ -703,7 +763,8 @@ __global__ void __launch_bounds__(kThreads, 1) fp8z_step_kernel(const StepArgs A
             // this point.
             if (k == 0 && staged) {
                 const BlockCtx* pc = ctx + ((i - 1) & 1);
-                if (!column_major_out(A, pc->bi, pc->pi, tile, tile_bar, tile_phase, wd, warp, lane)) return;
+                if (!column_major_out(A, pc->bi, pc->pi, tile, tout, tile_bar, tile_phase, wd, warp, lane))
+                    return;
                 staged = false;
             }
         }
@@ -741,7 +802,7 @@ __global__ void __launch_bounds__(kThreads, 1) fp8z_step_kernel(const StepArgs A
             const ParamInfo pi = c->pi;
             if (kRowMajor && bi.param >= 0) {
                 if (dest_ok(A, bi, pi, A.w_row_bytes, -1))
-                    store_rowmajor(A, bi, pi, words, warp, col);
+                    store_rowmajor(A, bi, pi, words, tout, warp, lane, col);
                 else if (tid == 0)
                     report_status(A.dev_status, FP8Z_EINVAL);
             }
@@ -754,7 +815,7 @@ __global__ void __launch_bounds__(kThreads, 1) fp8z_step_kernel(const StepArgs A
     }
     if (staged) {
         const BlockCtx* pc = ctx + ((nmine - 1) & 1);
-        column_major_out(A, pc->bi, pc->pi, tile, tile_bar, tile_phase, wd, warp, lane);
+        column_major_out(A, pc->bi, pc->pi, tile, tout, tile_bar, tile_phase, wd, warp, lane);
     }
 }
 
