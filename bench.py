@@ -243,6 +243,7 @@ def run_ours(args):
     wt = torch.empty(t_bytes, dtype=torch.uint8, device=dev) if w.transposed else None
     it = torch.empty(t_scales, dtype=torch.float32, device=dev) if w.transposed else None
     status = torch.zeros(1, dtype=torch.int32, device=dev)
+    torch.cuda.synchronize(dev)          # drawn on torch's stream; the steps run on their own
     stream = torch.cuda.Stream(dev)
     step0 = int(w.hp["step"])
     hp_kw = dict(w.hp)
@@ -529,12 +530,16 @@ def time_aux_kernels(w, q, inv, params, dev, stream, peak, reps=5, g=None, fused
 
 
 def _activation(T, Hd, dev, seed=5):
-    """An activation of T tokens x Hd: N(0,1) with 0.1 % outliers x60."""
+    """An activation of T tokens x Hd: N(0,1) with 0.1 % outliers x60.  Drawn
+    on torch's current stream; the device is synchronized before it is
+    returned, so kernels on another stream read it complete."""
     import torch
     gen = torch.Generator(device=dev)
     gen.manual_seed(seed)
     x = torch.randn(T, Hd, generator=gen, device=dev)
-    return torch.where(torch.rand(T, Hd, generator=gen, device=dev) < 1e-3, x * 60, x)
+    x = torch.where(torch.rand(T, Hd, generator=gen, device=dev) < 1e-3, x * 60, x)
+    torch.cuda.synchronize(dev)
+    return x
 
 
 def rowwise_study(dev, stream, peak, reps=5):
@@ -824,6 +829,7 @@ def run_configs(args, dev, stream, peak, reps=10):
         inv = torch.empty(cap, dtype=torch.float32, device=dev)
         desc = fp8z.table_to_device(blocks, dev)
         status = torch.zeros(1, dtype=torch.int32, device=dev)
+        torch.cuda.synchronize(dev)      # drawn on torch's stream; the steps run on their own
         hp = fp8z.hparams(**w.hp)
         ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
 
