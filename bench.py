@@ -328,7 +328,7 @@ def run_ours(args):
 
     torch.cuda.nvtx.range_push("aux_kernels")
     aux = None if (args.no_aux or len(shards) != 1) else time_aux_kernels(
-        w, q, inv, params, dev, stream, peak, g=state["g"], fused=fused)
+        w, q, inv, params, dev, stream, peak, g=state["g"], fused=fused, no_rowwise=args.no_rowwise)
     torch.cuda.nvtx.range_pop()
     if aux is not None:
         # the MXFP8 output variant of the same step (no column-major copy): codes
@@ -449,7 +449,7 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
-def time_aux_kernels(w, q, inv, params, dev, stream, peak, reps=5, g=None, fused=None):
+def time_aux_kernels(w, q, inv, params, dev, stream, peak, reps=5, g=None, fused=None, no_rowwise=False):
     """Dequantize, the standalone column-major transpose, unfold/fold of the
     FP32 grad, the fused row-major step, unfold of the E4M3 codes, and the 1x128
     row-wise kernels (rowwise_study), each timed with CUDA events against its
@@ -522,10 +522,11 @@ def time_aux_kernels(w, q, inv, params, dev, stream, peak, reps=5, g=None, fused
         qb = torch.empty(E * H * W, dtype=torch.uint8, device=dev)
         timed(lambda: fp8z.fp8z_unfold(q, pe, qb, stream=stream), 2 * E * H * W, "fp8z_unfold_e4m3")
         del qb
-    try:
-        out.update(rowwise_study(dev, stream, peak))
-    except RuntimeError:
-        pass
+    if not no_rowwise:
+        try:
+            out.update(rowwise_study(dev, stream, peak))
+        except RuntimeError:
+            pass
     return out
 
 
@@ -620,7 +621,10 @@ def rowwise_error_study(x, stream):
     frac_codes_differ (codes of the two column-wise tensors), frac_values_differ
     and rel_mean_abs_E = sum|E| / sum|X| on the dequantized values (the two
     sides may carry different scales), for E_naive and for the scaling-aware
-    E_sa = SA(Q_row(X)) - Q_col(X)."""
+    E_sa = SA(Q_row(X)) - Q_col(X); and frac_changed_vs_row_*: the fraction of
+    values that moving to the column-wise layout changes from the row-wise
+    values D(Q_row(X))^T (the double quantization itself; with power-of-two
+    scales the scaling-aware transpose changes only values that underflow)."""
     import torch
     from blockwise_fp8_zero_gb300 import fp8z
     T, Hd = x.shape
@@ -651,12 +655,16 @@ def rowwise_error_study(x, stream):
             s_sa = torch.empty(Hd, T // 128, device=dev)
             fp8z.fp8z_transpose_rowwise(q_row, s_row, q_sa, s_sa, stream=stream)
             row = {}
+            v_row_t = dq(q_row, s_row, transpose=True)              # D(Q_row(X))^T
             for tag, (q2, s2) in (("naive", (q_nv, s_nv)), ("scaling_aware", (q_sa, s_sa))):
-                e = dq(q2, s2) - v_dir
+                v2 = dq(q2, s2)
+                e = v2 - v_dir
                 row[f"frac_codes_differ_{tag}"] = round(float((q2 != q_dir).double().mean()), 6)
                 row[f"frac_values_differ_{tag}"] = round(float((e != 0).double().mean()), 6)
                 row[f"rel_mean_abs_E_{tag}"] = round(float(e.abs().double().sum()) / denom, 7)
-                del e
+                row[f"frac_changed_vs_row_{tag}"] = round(float((v2 != v_row_t).double().mean()), 6)
+                del e, v2
+            del v_row_t
             # the row-wise values themselves against X (one quantization)
             row["rel_err_row_layout"] = round(float((dq(q_row, s_row) - x).abs().double().sum()) / denom, 6)
             res[name] = row
@@ -665,7 +673,8 @@ def rowwise_error_study(x, stream):
     res["param"] = f"{T}x{Hd} activation"
     res["note"] = ("E = Q_col(D(Q_row(X))) - Q_col(X) on dequantized values; rel_mean_abs_E = "
                    "sum|E| / sum|X|; *_scaling_aware: the same with the scaling-aware transpose in "
-                   "place of the naive path")
+                   "place of the naive path; frac_changed_vs_row_*: values that differ from "
+                   "D(Q_row(X))^T")
     return res
 
 
@@ -951,6 +960,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-aux", action="store_true", help="skip the dequant/transpose timings")
     ap.add_argument("--no-configs", action="store_true", help="skip the other workloads' step timings")
+    ap.add_argument("--no-rowwise", action="store_true", help="skip the 1x128 row-wise study")
     ap.add_argument("--max-elems", type=int, default=0,
                     help="run a smaller workload of the same kind (profiling cases)")
     args = ap.parse_args()
