@@ -273,7 +273,12 @@ FP8Z_API int fp8z_adamw_requant_step_rowmajor_static(
  * §3.1 (32-element blocks share an 8-bit exponent).  Shared exponent
  * x = floor(log2(amax)) - 8, clamped to [-127, 127] (0 for an all-zero
  * group); scale byte = x + 127; code = E4M3(p' / 2^x), nearest even,
- * saturating.  AdamW, padding, p/g/m/v/w_fp8/desc and errors as
+ * saturating.  This is the OCP MX rule (the group's largest binade goes to
+ * E4M3's largest, [256, 512)): a group whose largest element has a
+ * significand above 1.75 maps it into (448, 512) and saturates it to 448,
+ * up to ~12.5 % low, where the block-scaled step never saturates.  The
+ * block-scaled knobs hp->fp8_max, min_scale and scale_mode do not enter.
+ * AdamW, padding, p/g/m/v/w_fp8/desc and errors as
  * fp8z_adamw_requant_step.  mx_scale: device u8 [capacity_blocks, 128, 4]
  * (block b at b*512, row r at r*4), written byte by byte (no alignment
  * needed; nullptr is FP8Z_EINVAL).  Each block needs no block-wide amax, so

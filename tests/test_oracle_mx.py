@@ -119,3 +119,36 @@ def test_mx_padding_and_desc(oracle):
     s1 = sc[512:1024].reshape(128, 4)
     assert np.all(s1[72:] == 127)                           # padding rows: all-zero groups
     assert np.all(s1[:72, 3] != 127)                        # cols 96..99 of group 3 are real
+
+
+def test_mx_group_max_above_448_saturates_and_ignores_block_knobs(oracle):
+    """The shared exponent is floor(log2 amax) - 8 (the OCP MX rule: the largest
+    element's binade is put at E4M3's top binade, [256, 512)).  A group whose
+    largest element has significand above 1.75 therefore lands in (448, 512)
+    and saturates to the 448 code, up to ~12.5 % low; fp8_max and min_scale,
+    the block-scaled step's knobs, do not enter.  lr = 0 keeps p' = p, so the
+    group's values are set directly."""
+    rng = np.random.default_rng(4)
+    p, g, m, v = _state(rng, 1, spike=False)
+    row = 3
+    grp = p[row * 128 + 32: row * 128 + 64]                # row 3, group 1
+    grp[:] = rng.uniform(-1.0, 1.0, 32).astype(np.float32) * 2.0 ** -5
+    grp[17] = np.float32(1.9 * 2.0 ** -3)                   # significand 1.9 > 1.75, binade 2^-3
+    grp[4] = np.float32(-1.99 * 2.0 ** -4)                  # below the group max
+    runs = []
+    for kw in (dict(), dict(fp8_max=100.0, min_scale=1e3), dict(fp8_max=448.0, min_scale=0.0, scale_mode=1)):
+        hp = oracle.Hparams.make(lr=0.0, weight_decay=0.0, step=5, **kw)
+        a = [x.copy() for x in (p, g, m, v)]
+        q = np.zeros(BLK, np.uint8)
+        sc = np.zeros(512, np.uint8)
+        oracle.adamw_requant_step_mx(*a, q, sc, 0, 1, hp)
+        assert np.array_equal(a[0], p)                      # lr = 0: p' = p
+        runs.append((q, sc))
+    q, sc = runs[0]
+    assert sc[row * 4 + 1] == 127 + (-3 - 8)                # x = floor(log2(1.9 * 2^-3)) - 8 = -11
+    assert q[row * 128 + 32 + 17] == 0x7E                   # 1.9 * 2^8 = 486.4 -> saturates to 448
+    assert oracle.e4m3_decode(q[row * 128 + 32 + 17:row * 128 + 32 + 18])[0] * 2.0 ** -11 == 448 * 2.0 ** -11
+    # -1.99 * 2^-4 / 2^-11 = -254.72 -> nearest E4M3 (spacing 16 in [256, 512), 8 in [128, 256)): -256
+    assert q[row * 128 + 32 + 4] == 0xF8
+    for q2, s2 in runs[1:]:
+        assert np.array_equal(q2, q) and np.array_equal(s2, sc)
