@@ -159,6 +159,32 @@ def max_over_ranks(x: float, device=None) -> float:
     return float(t.item())
 
 
+def box_copy_gbs(dev, reps=10):
+    """The measured-peak recipe on this machine, after the timed region: b.copy_(a)
+    over 1 Gi bf16 elements, read + write bytes, best of `reps`, CUDA events.
+    Context for the box-to-box spread; the roofline's peak stays the
+    driver-written one."""
+    import torch
+    try:
+        a = torch.empty(1 << 30, dtype=torch.bfloat16, device=dev)
+        b = torch.empty_like(a)
+    except RuntimeError:
+        return None
+    a.fill_(1.0)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    best = None
+    for _ in range(reps + 1):
+        ev[0].record()
+        b.copy_(a)
+        ev[1].record()
+        torch.cuda.synchronize(dev)
+        ms = ev[0].elapsed_time(ev[1])
+        best = ms if best is None else min(best, ms)
+    del a, b
+    torch.cuda.empty_cache()
+    return 2 * (1 << 30) * 2 / (best / 1e3) / 1e9
+
+
 def host_mem_gb():
     try:
         for line in open("/proc/meminfo"):
@@ -326,9 +352,11 @@ def run_ours(args):
             dev_status=status, stream=stream), alg_bytes_step, "fp8z_adamw_requant_step_rowmajor")
         del w_row
 
+    box_copy = box_copy_gbs(dev)
     torch.cuda.nvtx.range_push("aux_kernels")
     aux = None if (args.no_aux or len(shards) != 1) else time_aux_kernels(
-        w, q, inv, params, dev, stream, peak, g=state["g"], fused=fused, no_rowwise=args.no_rowwise)
+        w, q, inv, params, dev, stream, peak, g=state["g"], fused=fused, no_rowwise=args.no_rowwise,
+        max_tokens=args.rowwise_max_tokens)
     torch.cuda.nvtx.range_pop()
     if aux is not None:
         # the MXFP8 output variant of the same step (no column-major copy): codes
@@ -432,6 +460,8 @@ def run_ours(args):
                      "frac": round(achieved / peak, 4), "traffic": traffic,
                      "algorithmic_bytes": alg_bytes_step // launches_per_step,
                      "peak_source": peak_src,
+                     "box_copy_gbs": None if box_copy is None else round(box_copy, 1),
+                     "frac_of_box_copy": None if box_copy is None else round(achieved / box_copy, 4),
                      "kernel": "fp8z_step_kernel", "kernel_ms": round(avg_launch_s * 1e3, 4)},
         "aux_kernels": aux,
         "shard_timing": shard_timing,
@@ -449,7 +479,8 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
-def time_aux_kernels(w, q, inv, params, dev, stream, peak, reps=5, g=None, fused=None, no_rowwise=False):
+def time_aux_kernels(w, q, inv, params, dev, stream, peak, reps=5, g=None, fused=None, no_rowwise=False,
+                     max_tokens=65536):
     """Dequantize, the standalone column-major transpose, unfold/fold of the
     FP32 grad, the fused row-major step, unfold of the E4M3 codes, and the 1x128
     row-wise kernels (rowwise_study), each timed with CUDA events against its
@@ -524,7 +555,7 @@ def time_aux_kernels(w, q, inv, params, dev, stream, peak, reps=5, g=None, fused
         del qb
     if not no_rowwise:
         try:
-            out.update(rowwise_study(dev, stream, peak))
+            out.update(rowwise_study(dev, stream, peak, max_tokens=max_tokens))
         except RuntimeError:
             pass
     return out
@@ -543,7 +574,7 @@ def _activation(T, Hd, dev, seed=5):
     return x
 
 
-def rowwise_study(dev, stream, peak, reps=5):
+def rowwise_study(dev, stream, peak, reps=5, max_tokens=65536):
     """1x128 row-wise quantization and the two ways to the column-wise layout
     ("FP8-Flow-MoE" §3.1): the scaling-aware transpose, and the naive
     dequantize -> transpose -> quantize, both run from the library's kernels
@@ -575,7 +606,8 @@ def rowwise_study(dev, stream, peak, reps=5):
 
     Hd = 7168
     sweep = {}
-    for T in (4096, 16384, 65536):
+    tokens = [T for T in (4096, 16384, 65536) if T <= max_tokens] or [4096]
+    for T in tokens:
         x = _activation(T, Hd, dev)
         n = T * Hd
         qa = torch.empty(T, Hd, dtype=torch.uint8, device=dev)
@@ -588,7 +620,7 @@ def rowwise_study(dev, stream, peak, reps=5):
         ms_dt = timed(lambda: fp8z.fp8z_dequant_rowwise(qa, sa, xt, transpose=True, stream=stream))
         ms_qt = timed(lambda: fp8z.fp8z_quantize_rowwise(xt, True, qta, sta, stream=stream))
         param = f"{T}x{Hd} activation"
-        if T == 65536:
+        if T == tokens[-1]:
             out["fp8z_quantize_rowwise"] = entry(ms_q, 5 * n + 4 * n // 128, param)
             out["fp8z_transpose_rowwise"] = entry(ms_sa, 2 * n + 8 * n // 128, param)
             out["fp8z_dequant_rowwise_transposed"] = entry(ms_dt, 5 * n + 4 * n // 128, param)
@@ -596,15 +628,15 @@ def rowwise_study(dev, stream, peak, reps=5):
                          "naive_dequant_transpose_requant_ms": round(ms_dt + ms_qt, 4),
                          "naive_over_scaling_aware": round((ms_dt + ms_qt) / ms_sa, 3)}
         del qa, sa, qta, sta, xt
-        if T != 65536:
+        if T != tokens[-1]:
             del x
     out["rowwise_transpose_speed"] = {
         "by_tokens": sweep,
         "note": "T x 7168 activations, power-of-two scales; naive = fp8z_dequant_rowwise (transposed "
                 "output) + fp8z_quantize_rowwise; the page reports 2-3x for its direct transpose "
                 "over dequantize-transpose-quantize (\"FP8-Flow-MoE\" §3.1, Figure 1)"}
-    out["naive_dequant_transpose_requant_ms"] = sweep["65536"]["naive_dequant_transpose_requant_ms"]
-    out["naive_over_scaling_aware"] = sweep["65536"]["naive_over_scaling_aware"]
+    out["naive_dequant_transpose_requant_ms"] = sweep[str(tokens[-1])]["naive_dequant_transpose_requant_ms"]
+    out["naive_over_scaling_aware"] = sweep[str(tokens[-1])]["naive_over_scaling_aware"]
     out["rowwise_double_quantization"] = rowwise_error_study(x, stream)
     del x
     return out
@@ -961,6 +993,8 @@ def main():
     ap.add_argument("--no-aux", action="store_true", help="skip the dequant/transpose timings")
     ap.add_argument("--no-configs", action="store_true", help="skip the other workloads' step timings")
     ap.add_argument("--no-rowwise", action="store_true", help="skip the 1x128 row-wise study")
+    ap.add_argument("--rowwise-max-tokens", type=int, default=65536,
+                    help="largest activation of the row-wise study (4096, 16384 or 65536 tokens)")
     ap.add_argument("--max-elems", type=int, default=0,
                     help="run a smaller workload of the same kind (profiling cases)")
     args = ap.parse_args()
