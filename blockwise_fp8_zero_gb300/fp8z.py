@@ -18,6 +18,7 @@ LIB_PATH = os.path.join(_PKG, "libfp8z.so")
 
 BLOCK = 128
 BLOCK_ELEMS = BLOCK * BLOCK
+STATIC_GRAD_MAPS = 1024      # FP8Z_STATIC_GRAD_MAPS: params the no-allocation row-major step takes
 
 FP8Z_OK, FP8Z_EINVAL, FP8Z_EALIGN, FP8Z_ENOSPACE = 0, -1, -2, -3
 FP8Z_ECUDA, FP8Z_ETIMEOUT, FP8Z_EUNSUPPORTED = -4, -5, -6
@@ -329,6 +330,9 @@ def fp8z_adamw_requant_step_rowmajor_static(p, m, v, grads, params_host, w_row, 
     ent = np.ascontiguousarray(params_host, dtype=param_entry_dtype)
     if len(grads) != int(nparams) or len(ent) != int(nparams):
         raise ValueError("one grad and one host param entry per param")
+    if int(nparams) > STATIC_GRAD_MAPS:
+        raise ValueError(f"{int(nparams)} params: the library's map array holds at most "
+                         f"{STATIC_GRAD_MAPS}; use fp8z_adamw_requant_step_rowmajor with a g_maps buffer")
     for gt, pe in zip(grads, ent):
         if gt.dtype != torch.float32 or gt.numel() < int(pe["e"]) * int(pe["rows"]) * int(pe["cols"]):
             raise ValueError("grad must be float32 and hold the whole param")
