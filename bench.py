@@ -846,6 +846,76 @@ CONFIG_RUNS = [("single_256x384", None), ("dense_h7168", None), ("moe64", None),
                ("mixed500", 1), ("mixed500", 0)]
 
 
+def _measure_config(w, dev, stream, peak, reps):
+    """One workload of run_configs: plan, draw, time, free (its tensors go out of
+    scope on return)."""
+    import torch
+    from blockwise_fp8_zero_gb300 import fp8z, workloads
+    params, shards, blocks, summ = fp8z.fp8z_plan_shards(w.shapes, w.dp, w.split)
+    cap = int(summ["capacity_blocks"])
+    free, _ = torch.cuda.mem_get_info(dev)
+    if cap * BLK * 17 + (4 << 30) > free:
+        return {"skipped": f"needs {cap * BLK * 17 / 1e9:.0f} GB, {free / 1e9:.0f} GB free"}
+    state = workloads.make_state(w, blocks, dev, seed=0)
+    q = torch.empty(cap * BLK, dtype=torch.uint8, device=dev)
+    inv = torch.empty(cap, dtype=torch.float32, device=dev)
+    desc = fp8z.table_to_device(blocks, dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    torch.cuda.synchronize(dev)      # drawn on torch's stream; the steps run on their own
+    hp = fp8z.hparams(**w.hp)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+
+    def timed(ranges):
+        def go():
+            for b0, nb in ranges:
+                fp8z.fp8z_adamw_requant_step(state["p"], state["g"], state["m"], state["v"], q, inv, b0,
+                                             nb, hp, desc=desc, dev_status=status, stream=stream)
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                go()
+            ev[0].record(stream)
+            for _ in range(reps):
+                go()
+            ev[1].record(stream)
+        torch.cuda.synchronize(dev)
+        return ev[0].elapsed_time(ev[1]) / reps
+
+    shard_ranges = [(int(sh["blk_begin"]), int(sh["blk_count_real"])) for sh in shards]
+    real = int(summ["real_elems"])
+    nreal = int(summ["total_blocks"])
+    per_block = BLK * 29 + 24
+    ms = timed(shard_ranges)
+    entry = {"dp_shards": w.dp, "split": "param-wise" if w.split == 1 else "block-wise",
+             "params": len(w.shapes), "elements": real, "blocks": nreal, "capacity_blocks": cap,
+             "padding_bytes_fp32_state": int(summ["fold_pad_elems"] + summ["shard_pad_elems"]) * 16,
+             "fold_pad_elems": int(summ["fold_pad_elems"]),
+             "shard_pad_elems": int(summ["shard_pad_elems"]),
+             "launches": len(shards), "ms": round(ms, 4),
+             "gelem_s": round(real / (ms / 1e3) / 1e9, 4),
+             "gbs": round(nreal * per_block / ms / 1e6, 1),
+             "frac": round(nreal * per_block / ms / 1e6 / peak, 4)}
+    if len(shards) > 1:
+        one_ms = timed([(0, cap)])
+        a0, n0 = shard_ranges[0]
+        r0_ms = timed([(a0, n0)])
+        r0_real = int(np.sum(blocks["valid_rows"][a0:a0 + n0].astype(np.int64)
+                             * blocks["valid_cols"][a0:a0 + n0].astype(np.int64)))
+        entry["shard_timing"] = {
+            "per_shard_launches_ms": round(ms, 4),
+            "all_shards_one_launch_ms": round(one_ms, 4),
+            "all_shards_one_launch_gelem_s": round(real / (one_ms / 1e3) / 1e9, 4),
+            "all_shards_one_launch_frac": round(cap * per_block / one_ms / 1e6 / peak, 4),
+            "rank0_shard_ms": round(r0_ms, 4), "rank0_blocks": n0,
+            "rank0_gelem_s": round(r0_real / (r0_ms / 1e3) / 1e9, 4),
+            "rank0_gbs": round(n0 * per_block / r0_ms / 1e6, 1),
+            "rank0_frac": round(n0 * per_block / r0_ms / 1e6 / peak, 4)}
+    else:
+        entry["us"] = round(ms * 1e3, 2)
+    if status.item() != 0:
+        raise RuntimeError(f"{w.name}: {fp8z.fp8z_status_string(status.item())}")
+    return entry
+
+
 def run_configs(args, dev, stream, peak, reps=10):
     """The step on the other workloads, one after another in this process (each
     freed before the next): per-shard launches (the whole model's step as D
@@ -854,76 +924,15 @@ def run_configs(args, dev, stream, peak, reps=10):
     DP rank would run.  Bytes: 29 B per element of every block a launch
     processes (16 read, 13 written) + 24 B per block (descriptor, scale)."""
     import torch
-    from blockwise_fp8_zero_gb300 import fp8z, workloads
+    from blockwise_fp8_zero_gb300 import workloads
     res = {}
     for name, split in CONFIG_RUNS:
         w = workloads.get(name, split)
         key = name if split is None else f"{name}_{'paramwise' if split == 1 else 'blockwise'}"
-        params, shards, blocks, summ = fp8z.fp8z_plan_shards(w.shapes, w.dp, w.split)
-        cap = int(summ["capacity_blocks"])
-        free, _ = torch.cuda.mem_get_info(dev)
-        if cap * BLK * 17 + (4 << 30) > free:
-            res[key] = {"skipped": f"needs {cap * BLK * 17 / 1e9:.0f} GB, {free / 1e9:.0f} GB free"}
-            continue
-        state = workloads.make_state(w, blocks, dev, seed=0)
-        q = torch.empty(cap * BLK, dtype=torch.uint8, device=dev)
-        inv = torch.empty(cap, dtype=torch.float32, device=dev)
-        desc = fp8z.table_to_device(blocks, dev)
-        status = torch.zeros(1, dtype=torch.int32, device=dev)
-        torch.cuda.synchronize(dev)      # drawn on torch's stream; the steps run on their own
-        hp = fp8z.hparams(**w.hp)
-        ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
-
-        def timed(ranges):
-            def go():
-                for b0, nb in ranges:
-                    fp8z.fp8z_adamw_requant_step(state["p"], state["g"], state["m"], state["v"], q, inv, b0,
-                                                 nb, hp, desc=desc, dev_status=status, stream=stream)
-            with torch.cuda.stream(stream):
-                for _ in range(3):
-                    go()
-                ev[0].record(stream)
-                for _ in range(reps):
-                    go()
-                ev[1].record(stream)
-            torch.cuda.synchronize(dev)
-            return ev[0].elapsed_time(ev[1]) / reps
-
-        shard_ranges = [(int(sh["blk_begin"]), int(sh["blk_count_real"])) for sh in shards]
-        real = int(summ["real_elems"])
-        nreal = int(summ["total_blocks"])
-        per_block = BLK * 29 + 24
-        ms = timed(shard_ranges)
-        entry = {"dp_shards": w.dp, "split": "param-wise" if w.split == 1 else "block-wise",
-                 "params": len(w.shapes), "elements": real, "blocks": nreal, "capacity_blocks": cap,
-                 "padding_bytes_fp32_state": int(summ["fold_pad_elems"] + summ["shard_pad_elems"]) * 16,
-                 "fold_pad_elems": int(summ["fold_pad_elems"]),
-                 "shard_pad_elems": int(summ["shard_pad_elems"]),
-                 "launches": len(shards), "ms": round(ms, 4),
-                 "gelem_s": round(real / (ms / 1e3) / 1e9, 4),
-                 "gbs": round(nreal * per_block / ms / 1e6, 1),
-                 "frac": round(nreal * per_block / ms / 1e6 / peak, 4)}
-        if len(shards) > 1:
-            one_ms = timed([(0, cap)])
-            a0, n0 = shard_ranges[0]
-            r0_ms = timed([(a0, n0)])
-            r0_real = int(np.sum(blocks["valid_rows"][a0:a0 + n0].astype(np.int64)
-                                 * blocks["valid_cols"][a0:a0 + n0].astype(np.int64)))
-            entry["shard_timing"] = {
-                "per_shard_launches_ms": round(ms, 4),
-                "all_shards_one_launch_ms": round(one_ms, 4),
-                "all_shards_one_launch_gelem_s": round(real / (one_ms / 1e3) / 1e9, 4),
-                "all_shards_one_launch_frac": round(cap * per_block / one_ms / 1e6 / peak, 4),
-                "rank0_shard_ms": round(r0_ms, 4), "rank0_blocks": n0,
-                "rank0_gelem_s": round(r0_real / (r0_ms / 1e3) / 1e9, 4),
-                "rank0_gbs": round(n0 * per_block / r0_ms / 1e6, 1),
-                "rank0_frac": round(n0 * per_block / r0_ms / 1e6 / peak, 4)}
-        else:
-            entry["us"] = round(ms * 1e3, 2)
-        if status.item() != 0:
-            raise RuntimeError(f"{key}: {fp8z.fp8z_status_string(status.item())}")
-        res[key] = entry
-        del state, q, inv, desc, status
+        try:
+            res[key] = _measure_config(w, dev, stream, peak, reps)
+        except torch.cuda.OutOfMemoryError as e:
+            res[key] = {"skipped": f"out of device memory: {str(e).splitlines()[0][:120]}"}
         torch.cuda.empty_cache()
     res["note"] = ("no column-major copy (only the flat 6e9 workload carries one); the same kernel, "
                    "hyper-parameters of each workload; frac of the measured copy bandwidth")
