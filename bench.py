@@ -196,8 +196,9 @@ def host_mem_gb():
 
 
 # ----------------------------------------------------------- oracle (CPU)
-def cpu_oracle_run(w, host, hp_kw, threads):
-    """Time the oracle on host arrays (a block sample); returns seconds."""
+def cpu_oracle_run(w, host, hp_kw, threads, outputs=None):
+    """Time the oracle on host arrays (a block sample, updated in place); returns
+    seconds.  outputs: a dict that receives the oracle's codes and scales."""
     import oracle
     from concurrent.futures import ThreadPoolExecutor
     ohp = oracle.Hparams.make(**hp_kw)
@@ -215,7 +216,10 @@ def cpu_oracle_run(w, host, hp_kw, threads):
     t0 = time.perf_counter()
     with ThreadPoolExecutor(threads) as ex:
         list(ex.map(run, range(0, nb, per)))
-    return time.perf_counter() - t0
+    secs = time.perf_counter() - t0
+    if outputs is not None:
+        outputs["q"], outputs["inv"] = q, inv
+    return secs
 
 
 def sample_host_blocks(w, nblocks, seed=0):
@@ -471,7 +475,7 @@ def run_ours(args):
         "e2e": e2e,
     }
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:      # the host baseline at N = 1 only
-        line["cpu_baseline"] = cpu_baseline(w, hp_kw, args)
+        line["cpu_baseline"] = cpu_baseline(w, hp_kw, args, dev=dev)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if ws > 1:
@@ -939,11 +943,48 @@ def run_configs(args, dev, stream, peak, reps=10):
     return res
 
 
-def cpu_baseline(w, hp_kw, args, threads=None):
+def sample_parity(w, hp_kw, host_in, want, dev):
+    """The timed kernel on the oracle's block sample: the same inputs go through
+    fp8z_adamw_requant_step on the GPU, and every output is compared bit for bit
+    with the oracle's (p', m', v' as float bit patterns, NaN equal to NaN; E4M3
+    codes, a NaN code equal to either sign's; inverse scales)."""
+    import torch
+    from blockwise_fp8_zero_gb300 import fp8z
+    nb = host_in["p"].size // BLK
+    d = {k: torch.from_numpy(host_in[k]).to(dev) for k in "pgmv"}
+    q = torch.zeros(nb * BLK, dtype=torch.uint8, device=dev)
+    inv = torch.zeros(nb, dtype=torch.float32, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    fp8z.fp8z_adamw_requant_step(d["p"], d["g"], d["m"], d["v"], q, inv, 0, nb,
+                                 fp8z.hparams(**{**hp_kw, "step": int(hp_kw["step"])}), dev_status=st)
+    torch.cuda.synchronize(dev)
+    out = {"blocks": nb, "elements": nb * BLK, "status": int(st.item())}
+    for k in "pmv":
+        a = d[k].cpu().numpy()
+        b = want[k]
+        same = (a.view(np.uint32) == b.view(np.uint32)) | (np.isnan(a) & np.isnan(b))
+        out[f"{k}_mismatches"] = int((~same).sum())
+    qa, qb = q.cpu().numpy(), want["q"]
+    out["code_mismatches"] = int((~((qa == qb) | (((qa & 0x7F) == 0x7F) & ((qb & 0x7F) == 0x7F)))).sum())
+    out["scale_mismatches"] = int((inv.cpu().numpy().view(np.uint32) != want["inv"].view(np.uint32)).sum())
+    out["identical"] = out["status"] == 0 and not any(out[k] for k in
+                                                      ("p_mismatches", "m_mismatches", "v_mismatches",
+                                                       "code_mismatches", "scale_mismatches"))
+    return out
+
+
+def cpu_baseline(w, hp_kw, args, threads=None, dev=None):
     threads = threads or (os.cpu_count() or 1)
     nblocks = args.cpu_blocks
     host = sample_host_blocks(w, nblocks)
-    secs = cpu_oracle_run(w, host, {**hp_kw, "step": int(hp_kw["step"])}, threads)
+    host_in = {k: v.copy() for k, v in host.items()} if dev is not None else None
+    oracle_out = {}
+    secs = cpu_oracle_run(w, host, {**hp_kw, "step": int(hp_kw["step"])}, threads, outputs=oracle_out)
+    parity = None
+    if dev is not None:
+        parity = sample_parity(w, hp_kw, host_in, {"p": host["p"], "m": host["m"], "v": host["v"],
+                                                  "q": oracle_out["q"], "inv": oracle_out["inv"]}, dev)
+        del host_in
     # the same oracle on one core, on the first 1/16 of the sample
     n1 = max(1, nblocks // 16)
     one = {k: v[:n1 * BLK].copy() for k, v in host.items()}
@@ -954,7 +995,8 @@ def cpu_baseline(w, hp_kw, args, threads=None):
                       f"distributions, one oracle step, {threads} threads over block ranges, "
                       f"{secs:.2f} s wall",
             "single_core": {"value": round(n1 * BLK / secs1 / 1e9, 6), "unit": UNIT,
-                            "sample": f"{n1} blocks, {secs1:.2f} s wall"}}
+                            "sample": f"{n1} blocks, {secs1:.2f} s wall"},
+            "parity_vs_gpu": parity}
 
 
 def run_reference(args):
