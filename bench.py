@@ -388,6 +388,27 @@ def run_ours(args):
             del mx
         except RuntimeError:
             pass
+    if aux is not None and w.transposed:
+        # the same step without the column-major copy: what the copy costs on this machine
+        hp_nc = fp8z.hparams(**{**hp_kw, "step": t})
+        sh = shards[0]
+        ev3 = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        with torch.cuda.stream(stream):
+            run_nc = lambda: fp8z.fp8z_adamw_requant_step(
+                state["p"], state["g"], state["m"], state["v"], q, inv, int(sh["blk_begin"]),
+                int(sh["blk_count_real"]), hp_nc, desc=desc, dev_status=status, stream=stream)
+            run_nc()
+            ev3[0].record(stream)
+            for _ in range(5):
+                run_nc()
+            ev3[1].record(stream)
+        torch.cuda.synchronize(dev)
+        ms_nc = ev3[0].elapsed_time(ev3[1]) / 5
+        b_nc = nblk_run * (BLK * 29 + 24)
+        aux["fp8z_adamw_requant_step_nocopy"] = {"ms": round(ms_nc, 4), "bytes": b_nc,
+                                                 "gbs": round(b_nc / ms_nc / 1e6, 1),
+                                                 "frac": round(b_nc / ms_nc / 1e6 / peak, 4),
+                                                 "column_major_copy_ms": round(avg_launch_s * 1e3 - ms_nc, 4)}
     if aux and "fp8z_adamw_requant_step_rowmajor" in aux:
         aux["unfused_fold_step_unfold_ms"] = round(
             aux["fp8z_fold_f32"]["ms"] + avg_launch_s * 1e3 + aux["fp8z_unfold_e4m3"]["ms"], 4) \

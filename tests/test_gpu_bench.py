@@ -37,6 +37,8 @@ def test_bench_line_schema():
         assert k in r, k
     assert r["bound"] == "hbm" and r["unit"] == "GB/s" and 0 < r["frac"] < 1.5
     assert abs(r["frac"] - r["achieved"] / r["peak"]) < 1e-3
+    # the copy recipe re-measured on this machine, beside the recorded peak
+    assert r["box_copy_gbs"] > 0 and abs(r["frac_of_box_copy"] - r["achieved"] / r["box_copy_gbs"]) < 1e-3
     assert abs(d["value"] - d["config"]["elements"] / (d["ms_per_step"] / 1e3) / 1e9) < 0.01 * d["value"]
     assert d["gpu_launches"] == d["steps"]
     lo, hi = d["min_max_ms_per_step"]
