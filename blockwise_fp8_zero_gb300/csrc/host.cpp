@@ -77,7 +77,7 @@ int64_t wait_limit_ns() { return g_wait_limit_ns.load(std::memory_order_relaxed)
 
 namespace {
 constexpr int kMaxDevices = 64;
-constexpr int kMaxSlots = 10;
+constexpr int kMaxSlots = 12;
 std::atomic<int> g_smem_done[kMaxSlots][kMaxDevices];
 }  // namespace
 

@@ -326,10 +326,11 @@ FP8Z_API int fp8z_dequant(const uint8_t *w_fp8, const float *inv_scale, int64_t 
  *   at entry->blk_offset.
  * entry: HOST pointer to the param's planner entry (shape, hb, wb, blk_offset).
  * out: device u8 [e, cols, rows] (ld = rows); inv_scale_t: device f32
- *   [e, wb, hb].  out must be 16-byte aligned.  rows a multiple of 16: the
- *   blocks move through the TMA engine (persistent kernel, bounded waits);
- *   other row lengths take a one-CTA-per-block kernel with byte stores at
- *   unaligned edges.
+ *   [e, wb, hb].  out must be 16-byte aligned.  rows a multiple of 16: pairs
+ *   of vertically adjacent blocks move through the TMA engine and are written
+ *   as 256-byte row pieces (persistent kernel, bounded waits); other row
+ *   lengths take a one-CTA-per-block kernel with byte stores at unaligned
+ *   edges.
  * dev_status: nullable device int32, 4-byte aligned; FP8Z_ETIMEOUT lands
  *   there if a bounded wait of the TMA kernel gave up.
  * Returns FP8Z_OK / EINVAL / EALIGN / ECUDA.
