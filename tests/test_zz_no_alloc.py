@@ -97,3 +97,56 @@ def test_static_maps_step_matches_allocating_step_twice():
         # the step did run: the codes are not all zero
         assert int(new_out["w_row"].count_nonzero()) > t_bytes // 2, call
         del grads, maps
+
+
+@pytest.mark.gpu
+def test_static_maps_step_with_plain_load_grads():
+    """Grads whose row pitch is not a multiple of 16 bytes are described by
+    plain records instead of tensor maps; the library's array holds those
+    too.  Mixed with tensor-map params, one call, against the allocating
+    entry point."""
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from blockwise_fp8_zero_gb300 import build
+    build.build()
+    fp8z.lib()
+    dev = torch.device("cuda")
+    shapes = [(1, 300, 130), (1, 256, 384), (2, 129, 7)]
+    params, shards, blocks, summ = fp8z.fp8z_plan_shards(shapes, 1, 0)
+    cap = int(summ["capacity_blocks"])
+    t_bytes = int(sum(e * r * c for e, r, c in shapes))
+    desc = fp8z.table_to_device(blocks, dev)
+    pdev = fp8z.table_to_device(params, dev)
+    state = {}
+    for k, d in zip("pmv", (workloads.Dist("normal", 0.02), workloads.Dist("normal", 2e-4),
+                            workloads.Dist("uniform", 1e-7, 4e-7))):
+        t = torch.empty(cap * BLK)
+        workloads.fill(t, k, d, 5, blocks["valid_rows"], blocks["valid_cols"])
+        state[k] = t
+    gen = torch.Generator().manual_seed(9)
+    grads = [(torch.randn(s, generator=gen) * 1e-3).to(dev) for s in shapes]
+    hp = fp8z.hparams(step=3)
+    runs = []
+    for static in (False, True):
+        st = {k: state[k].to(dev) for k in "pmv"}
+        w_row = torch.zeros(t_bytes, dtype=torch.uint8, device=dev)
+        inv = torch.zeros(cap, device=dev)
+        status = torch.zeros(1, dtype=torch.int32, device=dev)
+        if static:
+            fp8z.fp8z_adamw_requant_step_rowmajor_static(st["p"], st["m"], st["v"], grads, params, w_row, inv, 0,
+                                                        cap, hp, desc, pdev, len(params), dev_status=status)
+        else:
+            maps = fp8z.fp8z_encode_grad_maps(grads, params)
+            fp8z.fp8z_adamw_requant_step_rowmajor(st["p"], st["m"], st["v"], maps, w_row, inv, 0, cap, hp, desc,
+                                                  pdev, len(params), dev_status=status)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        runs.append((st, w_row, inv))
+    (a, wa, ia), (b, wb, ib) = runs
+    for k in "pmv":
+        assert np.array_equal(a[k].cpu().numpy().view(np.uint32), b[k].cpu().numpy().view(np.uint32)), k
+    assert torch.equal(wa, wb)
+    data = blocks["param"] >= 0
+    assert np.array_equal(ia.cpu().numpy()[data].view(np.uint32), ib.cpu().numpy()[data].view(np.uint32))
+    assert int(wb.count_nonzero()) > t_bytes // 2
