@@ -280,7 +280,13 @@ __device__ __forceinline__ void tile_ratios(const float* s, int64_t i, int64_t j
 // (128B-swizzled loads and stores) reached 0.181 ms, and one that prefetched
 // the next strip into registers while writing the current one 0.175-0.196 ms
 // (two to four CTAs per SM), and one that staged the output words in plain
-// shared tiles written by one 2-D TMA tensor store each 0.20-0.26 ms: the
+// shared tiles written by one 2-D TMA tensor store each 0.20-0.26 ms, and
+// one that took two row tiles per CTA so that a lane re-expressed eight input
+// rows and a warp wrote 256 bytes of an output row per 8-byte store (half the
+// store instructions) 0.160-0.229 ms: with one column tile per CTA, four CTAs
+// per SM, 0.160 ms; with two, 69 KB of shared tiles per CTA left the SM's
+// carveout so little L1 for the staging loads in flight that they throttled
+// the memory pipe (0.229 ms at three CTAs per SM, 0.173 ms at two): the
 // re-expression arithmetic and the staging
 // loads' latency, not the memory system's bandwidth, set the pace.  The tile
 // loop stays
