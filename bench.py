@@ -871,6 +871,28 @@ CONFIG_RUNS = [("single_256x384", None), ("dense_h7168", None), ("moe64", None),
                ("mixed500", 1), ("mixed500", 0)]
 
 
+def _prior_moments(w, state, blocks, steps=10):
+    """m, v of a workload whose step count says it has run steps - 1 = 10
+    earlier steps: ten moment updates from zero (exp_avg = b1 exp_avg +
+    (1 - b1) g, exp_avg_sq = b2 exp_avg_sq + (1 - b2) g^2, the moment half of
+    the AdamW step), each with a fresh grad drawn from the workload's own grad
+    distribution, in plain torch ops on the device; the g buffer serves as the
+    scratch and gets the timed step's own grad back at the end.  The moments
+    do not depend on the params, so the params keep their draw."""
+    import torch
+    from blockwise_fp8_zero_gb300 import workloads
+    b1, b2 = float(w.hp["beta1"]), float(w.hp["beta2"])
+    vr, vc = blocks["valid_rows"], blocks["valid_cols"]
+    m, v, g = state["m"], state["v"], state["g"]
+    m.zero_()
+    v.zero_()
+    for k in range(steps):
+        workloads.fill(g, "g", w.dists["g"], 101 + k, vr, vc)
+        m.mul_(b1).add_(g, alpha=1.0 - b1)
+        v.mul_(b2).addcmul_(g, g, value=1.0 - b2)
+    workloads.fill(g, "g", w.dists["g"], 0, vr, vc)
+
+
 def _measure_config(w, dev, stream, peak, reps):
     """One workload of run_configs: plan, draw, time, free (its tensors go out of
     scope on return)."""
@@ -882,6 +904,9 @@ def _measure_config(w, dev, stream, peak, reps):
     if cap * BLK * 17 + (4 << 30) > free:
         return {"skipped": f"needs {cap * BLK * 17 / 1e9:.0f} GB, {free / 1e9:.0f} GB free"}
     state = workloads.make_state(w, blocks, dev, seed=0)
+    prior = int(w.extra.get("prior_steps", 0))
+    if prior > 0:
+        _prior_moments(w, state, blocks, prior)
     q = torch.empty(cap * BLK, dtype=torch.uint8, device=dev)
     inv = torch.empty(cap, dtype=torch.float32, device=dev)
     desc = fp8z.table_to_device(blocks, dev)
@@ -911,6 +936,8 @@ def _measure_config(w, dev, stream, peak, reps):
     per_block = BLK * 29 + 24
     ms = timed(shard_ranges)
     entry = {"dp_shards": w.dp, "split": "param-wise" if w.split == 1 else "block-wise",
+             "moments": (f"{prior} prior moment updates with fresh grads (plain torch ops)" if prior > 0
+                         else "zero (first step)"),
              "params": len(w.shapes), "elements": real, "blocks": nreal, "capacity_blocks": cap,
              "padding_bytes_fp32_state": int(summ["fold_pad_elems"] + summ["shard_pad_elems"]) * 16,
              "fold_pad_elems": int(summ["fold_pad_elems"]),

@@ -29,6 +29,8 @@ BLOCK_ELEMS = BLOCK * BLOCK
 # betas (0.9, 0.95): exp_avg is N(0, (0.2150*sigma)^2) since
 # Var = sigma^2 (1-b1)^2 sum_{j<10} b1^(2j); exp_avg_sq has mean
 # sigma^2 (1 - b2^10) = 0.4013 sigma^2, drawn here uniform in [0.5, 1.5] x mean.
+# Workloads drawn this way carry extra["prior_steps"] = 10, for a caller that
+# runs the ten moment updates itself instead.
 M10_STD = 0.2150
 V10_MEAN = 0.4013
 
@@ -87,17 +89,18 @@ def get(name: str, split: int | None = None) -> Workload:
         shapes = [(1, h, h), (1, h, h), (1, h, 576), (1, h, f), (1, h, f), (1, f, h)]
         return Workload(name, shapes, 8, 0, _hp(11),
                         dict(p=Dist("normal", 0.02), g=Dist("normal", 1e-3), **_ten_prior_steps(1e-3)),
-                        note="Q, O, KV-down, up, gate, down")
+                        note="Q, O, KV-down, up, gate, down", extra=dict(prior_steps=10))
     if name == "moe64":
         shapes = [(64, 2048, 7168), (64, 2048, 7168), (64, 7168, 2048)]
         sigma = 1e-3 * np.sqrt(3.0)          # std of 1e-3 * t(3)
         return Workload(name, shapes, 16, 0, _hp(11),
                         dict(p=Dist("normal", 0.02), g=Dist("student_t", 1e-3, 3.0),
                              **_ten_prior_steps(sigma)),
-                        note="gate, up, down banks of 64 experts")
+                        note="gate, up, down banks of 64 experts", extra=dict(prior_steps=10))
     if name == "mixed500":
         return Workload(name, mixed500_shapes(), 16, 1 if split is None else split, _hp(11),
-                        dict(p=Dist("normal", 0.02), g=Dist("normal", 1e-3), **_ten_prior_steps(1e-3)))
+                        dict(p=Dist("normal", 0.02), g=Dist("normal", 1e-3), **_ten_prior_steps(1e-3)),
+                        extra=dict(prior_steps=10))
     if name == "flat6e9":
         return Workload(name, [(117, 7168, 7168)], 1, 0, _hp(1000),
                         dict(p=Dist("normal", 0.02),

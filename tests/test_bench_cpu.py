@@ -28,3 +28,31 @@ def test_profiled_traffic_matches_current_kernel_or_is_null():
     import bench
     t = bench.profiled_traffic()
     assert t is None or 1.7e11 < t < 1.9e11
+
+
+def test_prior_moments_match_the_drawn_stand_in():
+    """The config timings run the ten moment updates that a step count of 11
+    implies; the parity tests draw m, v from the distribution those updates
+    give (exp_avg N(0, (0.2150 sigma)^2), exp_avg_sq of mean 0.4013 sigma^2).
+    The two must agree: on 64 blocks of N(0, 1e-3) grads the updates' m has
+    that spread and v that mean, within a sampling error of ~0.2 %.  Swapped
+    betas (v mean 0.651 sigma^2) or a missing (1 - beta) factor fail here."""
+    import numpy as np
+    import torch
+    sys.path.insert(0, ROOT)
+    import bench
+    from blockwise_fp8_zero_gb300 import workloads
+    w = workloads.get("dense_h7168")
+    assert w.extra["prior_steps"] == 10 and w.hp["step"] == 11
+    nb = 64
+    blocks = {"valid_rows": np.full(nb, 128, np.int32), "valid_cols": np.full(nb, 128, np.int32)}
+    state = {k: torch.full((nb * 16384,), 7.0) for k in "gmv"}
+    bench._prior_moments(w, state, blocks, 10)
+    sigma = 1e-3
+    m, v = state["m"].double(), state["v"].double()
+    assert abs(m.mean().item()) < 0.01 * workloads.M10_STD * sigma
+    assert abs(m.std().item() / (workloads.M10_STD * sigma) - 1) < 0.01
+    assert abs(v.mean().item() / (workloads.V10_MEAN * sigma * sigma) - 1) < 0.01
+    g0 = torch.empty(nb * 16384)
+    workloads.fill(g0, "g", w.dists["g"], 0, blocks["valid_rows"], blocks["valid_cols"])
+    assert torch.equal(state["g"], g0)          # the timed step's own grad is back
