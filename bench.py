@@ -872,14 +872,14 @@ CONFIG_RUNS = [("single_256x384", None), ("dense_h7168", None), ("moe64", None),
 
 
 def _prior_moments(w, state, blocks, steps=10):
-    """m, v of a workload whose step count says it has run steps - 1 = 10
-    earlier steps: ten moment updates from zero (exp_avg = b1 exp_avg +
-    (1 - b1) g, exp_avg_sq = b2 exp_avg_sq + (1 - b2) g^2, the moment half of
-    the AdamW step), each with a fresh grad drawn from the workload's own grad
-    distribution, in plain torch ops on the device; the g buffer serves as the
-    scratch and gets the timed step's own grad back at the end.  The moments
-    do not depend on the params, so the params keep their draw."""
-    import torch
+    """m, v of a workload that has run `steps` earlier optimizer steps (ten
+    for the step-11 workloads): that many moment updates from zero
+    (exp_avg = b1 exp_avg + (1 - b1) g, exp_avg_sq = b2 exp_avg_sq +
+    (1 - b2) g^2, the moment half of the AdamW step), each with a fresh grad
+    drawn from the workload's own grad distribution, in plain torch ops on the
+    tensors' device; the g buffer serves as the scratch and gets the timed
+    step's own grad back at the end.  The moments do not depend on the params,
+    so the params keep their draw."""
     from blockwise_fp8_zero_gb300 import workloads
     b1, b2 = float(w.hp["beta1"]), float(w.hp["beta2"])
     vr, vc = blocks["valid_rows"], blocks["valid_cols"]
