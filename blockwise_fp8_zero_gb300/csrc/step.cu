@@ -47,10 +47,7 @@ namespace {
 
 // Build-time shape of the pipeline.  The defaults won a sweep on GB300 at
 // 6e9 elements (28.0 ms per step): a deeper ring is faster (4 and 5 stages
-// lose 2-6 %) up to six stages (a seventh, which fits only where the copy's
-// two 16 KB tiles are not needed, ran 26.83 against 26.80 ms without the
-// copy and 27.34 against 27.25 ms for MXFP8), plain bulk loads beat the L2
-// evict-first hint (+1.5 %),
+// lose 2-6 %), plain bulk loads beat the L2 evict-first hint (+1.5 %),
 // streaming stores of the FP32 outputs help once the loads are plain, and
 // reading a block's column-major copy out of the shared tile during the next
 // block's first stage (instead of waiting for all warps right away) gains
