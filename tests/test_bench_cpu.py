@@ -61,3 +61,22 @@ def test_prior_moments_match_the_drawn_stand_in():
     g0 = torch.empty(nb * 16384)
     workloads.fill(g0, "g", w.dists["g"], 0, blocks["valid_rows"], blocks["valid_cols"])
     assert torch.equal(state["g"], g0)          # the timed step's own grad is back
+
+
+def test_reference_arm_under_torchrun_prints_one_line():
+    """Launched as the driver launches N > 1 (torchrun, one process per rank,
+    127.0.0.1), the reference arm runs on rank 0 alone: one JSON line with
+    n_gpus = 2, and every rank exits 0."""
+    import socket
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        port = sk.getsockname()[1]
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+           "--master-addr", "127.0.0.1", "--master-port", str(port), os.path.join(ROOT, "bench.py"),
+           "--impl", "reference", "--gpus", "2", "--steps", "2", "--warmup", "1", "--cpu-blocks", "32"]
+    out = subprocess.run(cmd, capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert out.returncode == 0, out.stderr[-2000:]
+    lines = [ln for ln in out.stdout.splitlines() if ln.strip().startswith("{")]
+    assert len(lines) == 1, out.stdout
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
