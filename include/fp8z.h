@@ -37,7 +37,8 @@
  *   - The device calls may be captured in a CUDA graph once the same call has
  *     run eagerly on the device (that first call sets the kernels' launch
  *     attributes); scalar arguments such as the hyper-parameters are captured
- *     by value.
+ *     by value.  fp8z_adamw_requant_step_rowmajor_static is the exception: it
+ *     uploads its grad maps from host memory that lives only for the call.
  */
 #ifndef FP8Z_H
 #define FP8Z_H
@@ -249,8 +250,8 @@ FP8Z_API int fp8z_adamw_requant_step_rowmajor(float *p, float *m, float *v, cons
  * fp8z_adamw_requant_step_rowmajor.
  * nparams > FP8Z_STATIC_GRAD_MAPS is refused with FP8Z_ENOSPACE, before any
  * device work.  The first call on a device looks up the array's device
- * address (cudaGetSymbolAddress, with that device current) and keeps it;
- * make that first call before any stream capture.  Every call shares the one
+ * address (cudaGetSymbolAddress, with that device current) and keeps it.
+ * It is not for stream capture (see the conventions above).  Every call shares the one
  * array per device: calls whose work overlaps on the GPU (for instance on two
  * streams) race on it, so issue them in one stream or order them.  The array
  * keeps the maps of the last call.  Calls neither cudaMalloc nor cudaFree nor
